@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark of the fa_fwd attention forward on GB300.
+
+One step = one forward pass (one fa_fwd launch) over the whole workload, with
+the inputs resident in HBM. Prints ONE JSON line (rank 0):
+
+  value         whole-job TFLOP/s (4*B*H*M*N*D per head pass, x1/2 when
+                causal), device-timed with CUDA events over exactly --steps
+                steps, barrier + synchronize on both sides, max over ranks.
+  e2e           the same metric through the public call with host buffers:
+                each step copies Q, K, V from pinned host memory, runs
+                fa_fwd, and copies O and LSE back.
+  roofline      the kernel's achieved TFLOP/s (per-launch CUDA events) against
+                the measured dense-BF16 peak.
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same
+                workload on this host's cores (rank 0 only).
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the oracle instead (the reference arm): each step
+is a bounded sample of the workload on the host cores.
+
+Multi-GPU (torchrun): every rank runs its own full replica of the workload
+(the work units are independent; there is no data exchange), so scaling is
+weak and ``value`` is the sum over ranks of the work divided by the slowest
+rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd attention TFLOP/s (4·B·H·M·N·D, causal ×½), % of BF16 tensor-core peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "causal_b8_h32_s4096_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 1 s of work)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU seconds for the oracle sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+            self._f = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self._f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    """Median SM clock, max clock and the throttle reasons seen (any sample)."""
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    reasons = set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for r in rows:
+        for name, val in zip(names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons), "samples": len(rows),
+            "power_w_max": max((num(r[3]) for r in rows if num(r[3]) is not None), default=None)}
+
+
+def clocks_rejected(clk) -> bool:
+    if any(r in BAD_REASONS for r in clk.get("reasons", [])):
+        return True
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return bool(sm and mx and sm < 0.5 * mx and not clk.get("reasons"))
+
+
+# --------------------------------------------------------- multi-rank glue
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def whole_job_value(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """TFLOP/s over all ranks: every rank does flops_per_step per step."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, target_s: float):
+    """Times the fp64 oracle on sampled query rows of head 0 of workload w.
+
+    Returns (TFLOP/s under the metric's convention, seconds, rows, cores,
+    description). The sample grows until it takes about target_s seconds.
+    """
+    import numpy as np
+
+    from flashattention_fa_fwd_gb300.inputs import head_tensor, sample_rows
+    from oracle import attention_rows
+
+    qh = head_tensor(w.wid, 0, 0, w.M, w.D, w.sigma_qk, w.dtype)
+    kh = head_tensor(w.wid, 1, 0, w.N, w.D, w.sigma_qk, w.dtype)
+    vh = head_tensor(w.wid, 2, 0, w.N, w.D, w.sigma_v, w.dtype)
+
+    def flops_of(rows):
+        vis = np.minimum(rows + 1, w.N) if w.causal else np.full(rows.size, w.N)
+        return 4.0 * w.D * float(vis.sum())
+
+    count = min(w.M, 32)
+    while True:
+        rows = sample_rows(w.wid, 0, w.M, count)
+        t0 = time.perf_counter()
+        attention_rows(qh, kh, vh, w.scale, w.causal, rows)
+        dt = time.perf_counter() - t0
+        if dt >= 0.25 * target_s or count >= w.M:
+            break
+        count = min(w.M, max(count * 2, int(count * 0.3 * target_s / max(dt, 1e-3))))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = f"{rows.size} sampled query rows of head 0 of {w.name} ({w.N} keys each, fp64 numpy)"
+    return flops_of(rows) / dt / 1e12, dt, int(rows.size), int(cores), desc
+
+
+def oracle_step_fn(w, rows_per_step: int):
+    """One reference-arm step: the oracle on a fixed sample of rows."""
+    import numpy as np
+
+    from flashattention_fa_fwd_gb300.inputs import head_tensor, sample_rows
+    from oracle import attention_rows
+
+    qh = head_tensor(w.wid, 0, 0, w.M, w.D, w.sigma_qk, w.dtype)
+    kh = head_tensor(w.wid, 1, 0, w.N, w.D, w.sigma_qk, w.dtype)
+    vh = head_tensor(w.wid, 2, 0, w.N, w.D, w.sigma_v, w.dtype)
+    rows = sample_rows(w.wid, 0, w.M, rows_per_step)
+    vis = np.minimum(rows + 1, w.N) if w.causal else np.full(rows.size, w.N)
+    flops = 4.0 * w.D * float(vis.sum())
+
+    def step():
+        attention_rows(qh, kh, vh, w.scale, w.causal, rows)
+
+    return step, flops, int(rows.size)
+
+
+def reference_arm(args, w, rank, world):
+    if rank != 0:
+        return 0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    steps = args.steps if args.steps is not None else 10
+    rows_per_step = min(w.M, 256)
+    step, flops, nrows = oracle_step_fn(w, rows_per_step)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = flops * steps / dt / 1e12
+    sample = f"each step: {nrows} sampled query rows of head 0 of {w.name} (fp64 numpy oracle)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), sample=sample),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, w, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from flashattention_fa_fwd_gb300.inputs import make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the fa_fwd arm")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    fa.load_library()
+    peaks = load_peaks()
+
+    bf16 = w.dtype == "bf16"
+    tdtype = torch.bfloat16 if bf16 else torch.float32
+    q_np, k_np, v_np = make_inputs(w)
+    hq, hk, hv = (torch.from_numpy(x).to(tdtype).pin_memory() for x in (q_np, k_np, v_np))
+    del q_np, k_np, v_np
+    q, k, v = (t.to(dev) for t in (hq, hk, hv))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.M, dtype=torch.float32, device=dev)
+    call = fa.fa_fwd if bf16 else fa.fa_fwd_f32
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        call(q, k, v, o, lse, w.scale, w.causal)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    # Calibrate the default step count to about one second of device time.
+    if args.steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        per = e0.elapsed_time(e1) / 5
+        steps = int(min(5000, max(20, math.ceil(1000.0 / max(per, 1e-3)))))
+        steps = int(max_over_ranks(float(steps), world, dev))
+    else:
+        steps = args.steps
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_begin.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    st = fa.fa_get_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after the timed region: {fa.fa_status_string(st)}")
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+    value = whole_job_value(w.flops, steps, world, max_ms)
+    launch_ms = statistics.mean(per_launch)
+    achieved = w.flops / (launch_ms * 1e-3) / 1e12
+
+    # End to end through the public call with host buffers.
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        call(q, k, v, o, lse, w.scale, w.causal)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1), world, dev)
+    e2e_value = whole_job_value(w.flops, args.e2e_steps, world, e2e_ms)
+    assert bool(torch.isfinite(hl).all()), "non-finite LSE in the end-to-end result"
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peak = float(peaks["bf16_tflops"])
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, secs, nrows, cores, desc = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+    in_bytes = h2d
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": max_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
+        "config": dict(w.describe(), parallelism=f"replicas x{world}",
+                       l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
+                       if in_bytes > 129e6 else "inputs fit in L2 (warm)"),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peaks.get('source')} bf16_tflops (burst); sustained "
+                                    f"{peaks.get('bf16_tflops_sustained')}",
+                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                     "launch_ms": launch_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps},
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "clocks_rejected": clocks_rejected(clocks),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from flashattention_fa_fwd_gb300.inputs import WORKLOADS
+
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
+    w = WORKLOADS[args.workload]
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, w, rank, world)
+    return gpu_arm(args, w, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

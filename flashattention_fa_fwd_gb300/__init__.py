@@ -1,0 +1,12 @@
+"""fa_fwd: a FlashAttention forward pass for one NVIDIA GB300 GPU (sm_103a).
+
+The computation lives in ``libfa_fwd.so`` (hand-written CUDA: a tcgen05 /
+TMA kernel for bf16 and an exact-fp32 CUDA-core kernel), behind the C ABI of
+``include/fa_fwd.h``. This package is its thin Python binding plus the seeded
+input generator the tests and the benchmark share. Importing it does not load
+the library; the first call does, and raises if it has not been built.
+"""
+
+from ._binding import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK,  # noqa: F401
+                       FaError, fa_fwd, fa_fwd_f32, fa_fwd_f32_raw, fa_fwd_raw, fa_get_device_status,
+                       fa_last_error, fa_status_string, library_path, load_library)

@@ -1,0 +1,178 @@
+"""ctypes binding of libfa_fwd.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/fa_fwd.h).
+The ``*_raw`` forms take integer device addresses and sizes exactly as the
+C ABI does; the plain forms take torch tensors, check them, and pass their
+pointers, shapes and the current CUDA stream. Every step of the attention
+computation runs in the library's CUDA kernels; there is no fallback. If the
+library is not built, the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa_fwd.so")
+_lock = threading.Lock()
+_lib = None
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error")
+
+
+class FaError(RuntimeError):
+    """A non-OK status from libfa_fwd.so."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = load_library()
+        name = lib.fa_status_string(status).decode()
+        detail = lib.fa_last_error().decode()
+        super().__init__(f"{where}: {name}: {detail}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libfa_fwd.so (once) and declares the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is not built; run `python -m flashattention_fa_fwd_gb300.build` "
+                "(or __graft_entry__.build()) with the CUDA 13 toolkit first")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        for name in ("fa_fwd", "fa_fwd_f32"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+            fn.restype = ctypes.c_int
+        lib.fa_get_device_status.argtypes = [vp]
+        lib.fa_get_device_status.restype = ctypes.c_int
+        lib.fa_status_string.argtypes = [ctypes.c_int]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_error.argtypes = []
+        lib.fa_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ raw ABI
+
+def fa_fwd_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+               scale: float, causal: bool, stream: int = 0) -> int:
+    """Calls fa_fwd with raw device addresses; returns the status code."""
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
+
+
+def fa_fwd_f32_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+                   scale: float, causal: bool, stream: int = 0) -> int:
+    """Calls fa_fwd_f32 with raw device addresses; returns the status code."""
+    return load_library().fa_fwd_f32(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(status).decode()
+
+
+def fa_last_error() -> str:
+    return load_library().fa_last_error().decode()
+
+
+# ------------------------------------------------------------ torch tensors
+
+def _shape4(t, name):
+    if t.dim() == 2:
+        return (1, 1) + tuple(t.shape)
+    if t.dim() == 4:
+        return tuple(t.shape)
+    raise ValueError(f"{name} must be [M, D] or [B, H, M, D], got {tuple(t.shape)}")
+
+
+def _marshal(q, k, v, o, lse, dtype):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 CUDA tensor")
+    B, H, M, D = _shape4(q, "q")
+    Bk, Hk, N, Dk = _shape4(k, "k")
+    if (Bk, Hk, Dk) != (B, H, D) or _shape4(v, "v") != (B, H, N, D):
+        raise ValueError("k and v must be [B, H, N, D] matching q's B, H and D")
+    if _shape4(o, "o") != (B, H, M, D):
+        raise ValueError("o must have q's shape")
+    if lse.numel() != B * H * M:
+        raise ValueError("lse must hold B*H*M values")
+    devs = {t.device for t in (q, k, v, o, lse)}
+    if len(devs) != 1:
+        raise ValueError("all tensors must be on the same device")
+    return B, H, M, N, D
+
+
+def _stream_of(t, stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool = False, stream=None) -> None:
+    """bf16 attention forward: writes ``o`` (bf16) and ``lse`` (fp32).
+
+    q [B, H, M, D] (or [M, D]), k and v [B, H, N, D], o like q, lse with
+    B*H*M fp32 values; all contiguous CUDA tensors on one device. Runs on
+    ``stream`` (default: the current torch stream) and does not synchronise.
+    """
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.bfloat16)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, M, N, D, scale, causal, _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+
+
+def fa_fwd_f32(q, k, v, o, lse, scale: float, causal: bool = False, stream=None) -> None:
+    """fp32 attention forward (CUDA cores, exact fp32): writes ``o`` and ``lse``."""
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.float32)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_f32_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, M, N, D, scale, causal, _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_f32")
+
+
+def fa_get_device_status(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream(dev).cuda_stream if stream is None else (
+            stream if isinstance(stream, int) else stream.cuda_stream)
+        return load_library().fa_get_device_status(s)

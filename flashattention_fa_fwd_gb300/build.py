@@ -1,0 +1,94 @@
+"""Builds libfa_fwd.so in-tree with nvcc for sm_103a.
+
+Each CUDA translation unit is compiled to an object file in parallel, then
+linked into ``flashattention_fa_fwd_gb300/libfa_fwd.so`` (static CUDA
+runtime; the tensor-map encoder is fetched from the driver at run time, so
+there is no libcuda link). Objects go to ``_build/`` at the repository root.
+A build is skipped when the library is newer than every source and was built
+for this machine's architecture.
+"""
+
+from __future__ import annotations
+
+import os
+import platform
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG_DIR)
+CSRC = os.path.join(PKG_DIR, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(ROOT, "_build")
+LIB_PATH = os.path.join(PKG_DIR, "libfa_fwd.so")
+STAMP = os.path.join(BUILD_DIR, "libfa_fwd.arch")
+
+SOURCES = ["fa_api.cu", "fa_f32.cu", "fa_bf16_d64.cu", "fa_bf16_d96.cu", "fa_bf16_d128.cu"]
+GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+              "-Xptxas", "-v"]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libfa_fwd.so")
+
+
+def _deps():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "fa_fwd.h"))
+    files.append(os.path.abspath(__file__))
+    return files
+
+
+def _up_to_date() -> bool:
+    if not (os.path.exists(LIB_PATH) and os.path.exists(STAMP)):
+        return False
+    with open(STAMP) as f:
+        if f.read().strip() != platform.machine():
+            return False
+    t = os.path.getmtime(LIB_PATH)
+    return all(os.path.getmtime(p) <= t for p in _deps())
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles and links libfa_fwd.so; returns its path."""
+    if not force and _up_to_date():
+        return LIB_PATH
+    nvcc = _nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+
+    def compile_one(src: str):
+        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *GENCODE, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        return src, obj, r
+
+    with ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    logs = []
+    for src, obj, r in results:
+        logs.append(f"== {src}\n{r.stdout}{r.stderr}")
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    with open(os.path.join(BUILD_DIR, "ptxas.log"), "w") as f:
+        f.write("\n".join(logs))
+    tmp = LIB_PATH + ".tmp"
+    cmd = [nvcc, *GENCODE, "-shared", "-o", tmp, *[o for _, o, _ in results], "-cudart", "static"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    with open(STAMP, "w") as f:
+        f.write(platform.machine())
+    if verbose:
+        print("\n".join(logs))
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,251 @@
+// Host side of libfa_fwd.so: the C ABI declared in include/fa_fwd.h.
+//
+// Validates arguments before anything touches the GPU, builds the TMA
+// tensor maps, picks the kernel for the head dimension and launches it on
+// the caller's stream. The library never synchronises inside fa_fwd /
+// fa_fwd_f32 and allocates nothing per call; the only allocation is one
+// 4-byte status word per device, made on the first call on that device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "fa_fwd.h"
+#include "fa_internal.h"
+
+#define FA_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_word[kMaxDevices] = {};
+int g_arch[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device set-up on first use: architecture check, status word, and the
+// driver's tensor-map encoder (fetched through the runtime, so the library
+// does not link libcuda).
+fa_status device_setup(bool need_encoder, uint32_t** status_word) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_arch[dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_arch[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch[dev] != 1) return fail(FA_ERR_UNSUPPORTED, "device %d is not sm_103 (this library is built for sm_103a only)", dev);
+    if (g_status_word[dev] == nullptr) {
+        uint32_t* w = nullptr;
+        e = cudaMalloc(&w, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
+        e = cudaMemset(w, 0, sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            cudaFree(w);
+            return cuda_fail(e, "clearing the status word");
+        }
+        g_status_word[dev] = w;
+    }
+    if (need_encoder && g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *status_word = g_status_word[dev];
+    return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    if (abytes <= 0 || bbytes <= 0 || a == nullptr || b == nullptr) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+// Shape and pointer checks shared by both entry points. Sets *empty when
+// there is nothing to compute.
+fa_status validate(const void* q, const void* k, const void* v, const void* o, const void* lse, int64_t B,
+                   int64_t H, int64_t M, int64_t N, int64_t D, float scale, int64_t elem, bool* empty) {
+    if (B < 0 || H < 0 || M < 0 || N < 0) return fail(FA_ERR_INVALID_ARG, "B, H, M and N must be >= 0");
+    if (D < 1) return fail(FA_ERR_INVALID_ARG, "D must be >= 1 (got %lld)", (long long)D);
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", (double)scale);
+    const int64_t kInt = 0x7fffffff;
+    if (B > kInt || H > kInt || M > kInt || N > kInt || D > kInt || (H > 0 && B > kInt / H))
+        return fail(FA_ERR_INVALID_ARG, "sizes exceed the 32-bit index range");
+    const int64_t bh = B * H;
+    // byte counts must fit in int64
+    const int64_t lim = INT64_MAX / 16;
+    if ((bh > 0 && M > lim / bh) || (bh > 0 && N > lim / bh) || (bh * M > 0 && D > lim / (bh * M)) ||
+        (bh * N > 0 && D > lim / (bh * N)))
+        return fail(FA_ERR_INVALID_ARG, "tensor sizes overflow");
+    const int64_t qbytes = bh * M * D * elem, kvbytes = bh * N * D * elem, lbytes = bh * M * 4;
+    *empty = (bh == 0 || M == 0);
+    if (*empty) return FA_OK;
+    if (q == nullptr || o == nullptr || lse == nullptr) return fail(FA_ERR_INVALID_ARG, "q, o and lse must not be null");
+    if (N > 0 && (k == nullptr || v == nullptr)) return fail(FA_ERR_INVALID_ARG, "k and v must not be null when N > 0");
+    if (!aligned(q, 16) || !aligned(o, 16) || (N > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+        return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (!aligned(lse, 4)) return fail(FA_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (overlaps(o, qbytes, q, qbytes) || overlaps(o, qbytes, k, kvbytes) || overlaps(o, qbytes, v, kvbytes) ||
+        overlaps(lse, lbytes, q, qbytes) || overlaps(lse, lbytes, k, kvbytes) || overlaps(lse, lbytes, v, kvbytes) ||
+        overlaps(o, qbytes, lse, lbytes))
+        return fail(FA_ERR_INVALID_ARG, "o and lse must not overlap the inputs or each other");
+    return FA_OK;
+}
+
+// 3-D {D, rows, B*H} bf16 map, 128-row x 64-column box, 128-byte swizzle.
+fa_status encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t bh, int64_t D) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(rows * D * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return FA_OK;
+}
+
+constexpr double kLog2e = 1.4426950408889634;
+
+}  // namespace
+
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                        int64_t M, int64_t N, int64_t D, float scale, int causal, void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 2, &empty);
+    if (st != FA_OK) return st;
+    if (D != 64 && D != 96 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "bf16 fa_fwd supports D in {64, 96, 128} (got %lld)", (long long)D);
+    if (empty) return FA_OK;
+    const int64_t bh = B * H;
+    const int64_t n_pairs = (M + 255) / 256;
+    if (bh * n_pairs > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many query tiles for one launch");
+    uint32_t* word = nullptr;
+    st = device_setup(true, &word);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
+    if (N > 0) {
+        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+    } else {
+        mk = mq;  // never read: no key tiles exist
+        mv = mq;
+    }
+    fa::Bf16Params p;
+    p.o = o;
+    p.lse = lse;
+    p.err = word;
+    p.bh_count = static_cast<int>(bh);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.n_pairs = static_cast<int>(n_pairs);
+    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (D) {
+        case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
+        case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
+        default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
+    return FA_OK;
+}
+
+FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t B,
+                            int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal, void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 4, &empty);
+    if (st != FA_OK) return st;
+    if (D > 128) return fail(FA_ERR_UNSUPPORTED, "fp32 fa_fwd_f32 supports D <= 128 (got %lld)", (long long)D);
+    if (empty) return FA_OK;
+    uint32_t* word = nullptr;
+    st = device_setup(false, &word);
+    if (st != FA_OK) return st;
+    fa::F32Params p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.bh_count = static_cast<int>(B * H);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    cudaError_t e = fa::launch_f32(p, causal != 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launching the fp32 kernel");
+    return FA_OK;
+}
+
+FA_API fa_status fa_get_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return FA_OK;
+    uint32_t* w;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        w = g_status_word[dev];
+    }
+    if (w == nullptr) return FA_OK;
+    uint32_t h = 0;
+    e = cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (h != 0) {
+        e = cudaMemset(w, 0, sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+        if (h & fa::DEV_ERR_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting on its pipeline (status 0x%x)", h);
+        return fail(FA_ERR_CUDA, "device status word 0x%x", h);
+    }
+    return FA_OK;
+}
+
+FA_API const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+FA_API const char* fa_last_error(void) { return g_msg; }

@@ -1,0 +1,53 @@
+// Internal interface between the host entry points (fa_api.cu) and the
+// kernel translation units. Not installed; not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Bits a kernel ORs into the per-device status word.
+constexpr uint32_t DEV_ERR_TIMEOUT = 1u;  // a pipeline wait ran out of time
+
+// Arguments of the bf16 tensor-core kernel that are not tensor maps.
+struct Bf16Params {
+    void* o;             // [BH, M, D] bf16
+    float* lse;          // [BH, M] fp32
+    uint32_t* err;       // device status word
+    int bh_count;        // B * H
+    int M;
+    int N;
+    int n_pairs;         // ceil(M / 256): units of two 128-row query tiles
+    int heads_per_group; // causal tile order: heads that share a group
+    float scale_log2;    // scale * log2(e)
+};
+
+// Launches the bf16 kernel for head dimension D (64, 96 or 128); the three
+// maps are 3-D {D, rows, B*H} bf16 maps with a {64, 128, 1} box and 128-byte
+// swizzle. Returns the launch error.
+cudaError_t launch_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const Bf16Params& p, bool causal, cudaStream_t s);
+cudaError_t launch_bf16_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const Bf16Params& p, bool causal, cudaStream_t s);
+cudaError_t launch_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                             const Bf16Params& p, bool causal, cudaStream_t s);
+
+// Arguments of the fp32 CUDA-core kernel.
+struct F32Params {
+    const float* q;
+    const float* k;
+    const float* v;
+    float* o;
+    float* lse;
+    int bh_count;
+    int M;
+    int N;
+    int D;
+    float scale_log2;
+};
+
+cudaError_t launch_f32(const F32Params& p, bool causal, cudaStream_t s);
+
+}  // namespace fa

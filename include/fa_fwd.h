@@ -1,0 +1,129 @@
+/*
+ * fa_fwd.h -- C ABI of libfa_fwd.so, the FlashAttention forward pass for one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation (what every entry point below computes)
+ * -----------------------------------------------------
+ * For every batch b < B and head h < H, with Q_bh an M x D matrix and K_bh,
+ * V_bh N x D matrices:
+ *
+ *     S   = scale * Q_bh K_bh^T                          (M x N, never stored)
+ *     S[i][j] = -inf where causal and j > i              (top-left causal mask)
+ *     O_bh[i]  = sum_j softmax_j(S[i]) * V_bh[j]          (M x D)
+ *     LSE_bh[i] = max_j S[i][j] + ln sum_j exp(S[i][j] - max_j S[i][j])
+ *
+ * Sources: attention as S = QK^T/sqrt(d), P = softmax(S), O = PV and the
+ * per-row log-sum-exp L = m + log(l) kept for the backward pass are from
+ * "Module 08: FlashAttention and Memory-Efficient Kernels" (sections "Where
+ * the time goes in standard attention" and "The backward pass: recompute
+ * instead of store"); the M-row query / N-row key problem statement and the
+ * caller-preallocated output are from "FlashAttention in Triton: A
+ * Tile-by-Tile Walkthrough" (sections "First, what does attention actually
+ * do?" and "Full Triton implementation"); the (batch, heads, sequence,
+ * head_dim) layout is the one of "Module 08" Code Step 7; the causal mask
+ * keeps key j for query i when j <= i as in "Module 08" Code Step 1. The
+ * pages show only square causal masks; for M != N this library keeps the
+ * same top-left rule (j <= i).
+ *
+ * A row with no visible key (only possible when N == 0) gets O = 0 and
+ * LSE = -inf. LSE is in natural-log units of the scaled scores.
+ *
+ * Layout and ownership (all entry points)
+ * ---------------------------------------
+ *   q   : [B, H, M, D] contiguous, device memory
+ *   k,v : [B, H, N, D] contiguous, device memory
+ *   o   : [B, H, M, D] contiguous, device memory, written
+ *   lse : [B, H, M]    contiguous fp32, device memory, written
+ * The caller allocates and owns every buffer; o and lse must not overlap
+ * the inputs or each other. `stream` is a cudaStream_t (NULL = the legacy
+ * default stream). Calls are asynchronous on `stream` and never
+ * synchronise; the results are ready when the stream reaches them.
+ *
+ * The library allocates nothing per call. On its first call on a device it
+ * allocates one 4-byte device status word for that device, which it keeps
+ * until the process exits; device-side failures (a pipeline wait that ran
+ * out of time) are OR-ed into that word and read by fa_get_device_status().
+ *
+ * Errors
+ * ------
+ * Arguments are checked on the host before anything is launched; a failed
+ * check launches nothing and returns:
+ *   FA_ERR_INVALID_ARG  a null pointer (unless the tensor it names is
+ *                       empty), B, H or M < 0, N < 0, D < 1, a scale that is
+ *                       not finite and > 0, a pointer that is not 16-byte
+ *                       aligned, or sizes whose byte counts overflow.
+ *   FA_ERR_UNSUPPORTED  a head dimension the entry point has no kernel for,
+ *                       or a current device that is not sm_103.
+ *   FA_ERR_CUDA         a CUDA runtime or driver call failed (details in
+ *                       fa_last_error()).
+ * B, H or M equal to 0 is a legal empty problem: nothing is launched and
+ * FA_OK is returned.
+ */
+#ifndef FA_FWD_H_
+#define FA_FWD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,
+    FA_ERR_UNSUPPORTED = 2,
+    FA_ERR_CUDA = 3,
+    FA_ERR_TIMEOUT = 4
+} fa_status;
+
+/*
+ * bf16 attention forward on the tensor cores (tcgen05, accumulators in
+ * tensor memory). q, k, v and o hold bf16 values; lse is fp32. Scores,
+ * the running max and sum and the output accumulator are fp32; the
+ * probabilities are rounded to bf16 before they multiply V (the pages'
+ * tutorial loop casts p to 16 bits for that product: "FlashAttention-style
+ * kernel", section "The loop").
+ *
+ * D must be 64, 96 or 128 (FA_ERR_UNSUPPORTED otherwise). The algorithm is
+ * the streaming softmax of "FlashAttention-style kernel" ("The loop", with
+ * its base-two exponent and log2(e) folded into the scale) with the
+ * FlashAttention-2 work split of "Module 08" (section "Related ideas"):
+ * each 128-row query tile stays on chip while 128-row key/value tiles
+ * stream past it, and causal key tiles that lie wholly above the diagonal
+ * are skipped ("FlashAttention-style kernel", section "Causal masking").
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                 float scale, int causal, void* stream);
+
+/*
+ * fp32 attention forward on the CUDA cores with exact fp32 fused
+ * multiply-adds (no TF32): the single-head fp32 problem of "FlashAttention
+ * in Triton: A Tile-by-Tile Walkthrough" (its kernel computes its dots in
+ * IEEE fp32), generalised to [B, H] and the causal mask. All buffers fp32.
+ * D must be in [1, 128].
+ */
+fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                     int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                     float scale, int causal, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns FA_ERR_TIMEOUT if a kernel launched since the last call gave
+ * up on a pipeline wait (its outputs are then undefined), FA_ERR_CUDA if the
+ * synchronisation itself failed, FA_OK otherwise.
+ */
+fa_status fa_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/* Detail of the last non-OK status returned on the calling thread (static
+ * per-thread buffer, valid until the thread's next call into the library). */
+const char* fa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_FWD_H_ */

@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA kernels, called through the C ABI binding, against
+the fp64 oracle on the same seeded inputs.
+
+Small and odd shapes are compared element by element on every output; the
+full-size attention workloads run in the launch configuration the benchmark
+times and are compared on sampled heads and rows (every output of the
+ragged cross-attention workload), plus properties that hold at any size.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention, attention_rows
+from flashattention_fa_fwd_gb300.inputs import WORKLOADS, head_tensor, make_inputs, round_to_bf16, sample_rows
+from parity import check_bf16, check_f32, run_bf16, run_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import flashattention_fa_fwd_gb300 as fa
+
+    fa.load_library()
+
+
+def _rand(shape, seed, sigma=1.0, bf16=True):
+    x = np.random.default_rng(seed).standard_normal(shape, dtype=np.float32) * np.float32(sigma)
+    return round_to_bf16(x) if bf16 else x
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_f32_single_head_workload():
+    w = WORKLOADS["f32_single_head_m256_n512_d64"]
+    q, k, v = make_inputs(w)
+    o, lse = run_f32(q, k, v, w.scale, w.causal)
+    o_ref, lse_ref = attention(q, k, v, w.scale, w.causal)
+    check_f32(o, lse, o_ref, lse_ref, w.name)
+
+
+@pytest.mark.parametrize("M,N,D", [(7, 13, 8), (35, 67, 32), (64, 129, 128), (1, 1, 1), (100, 3, 17)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_odd_sizes(M, N, D, causal):
+    """The odd sizes the Triton walkthrough checks ("What the H100 run
+    showed"), and degenerate ones, with and without the causal mask."""
+    q, k, v = (_rand((1, 2, r, D), 10 * M + N + i, bf16=False) for i, r in enumerate((M, N, N)))
+    o, lse = run_f32(q, k, v, 1 / math.sqrt(D), causal)
+    o_ref, lse_ref = attention(q, k, v, 1 / math.sqrt(D), causal)
+    check_f32(o, lse, o_ref, lse_ref, f"f32 {M}x{N}x{D} causal={causal}")
+
+
+def test_f32_worked_example():
+    """Scores [1, 2, 3], values [10, 20, 30] ("FlashAttention in Triton",
+    worked example): output 25.752 to the page's three decimals."""
+    q = np.array([[[[1.0]]]], dtype=np.float32)
+    k = np.array([[[[1.0], [2.0], [3.0]]]], dtype=np.float32)
+    v = np.array([[[[10.0], [20.0], [30.0]]]], dtype=np.float32)
+    o, lse = run_f32(q, k, v, 1.0, False)
+    assert abs(o[0, 0, 0, 0] - 25.752) <= 5e-4
+    assert abs(lse[0, 0, 0] - (3.0 + math.log(1.503))) <= 5e-4
+
+
+# ------------------------------------------------------------------ bf16 path
+
+@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("M,N", [(300, 700), (600, 600), (128, 128), (257, 129), (1, 200), (200, 1)])
+def test_bf16_shapes(D, causal, M, N):
+    """Several 128-row tiles, ragged M and N tails, single-row and single-key
+    problems, M != N under the top-left causal rule."""
+    B, H = 2, 3
+    q = _rand((B, H, M, D), 1 + M + 7 * N + D)
+    k = _rand((B, H, N, D), 2 + M + 7 * N + D)
+    v = _rand((B, H, N, D), 3 + M + 7 * N + D)
+    scale = 1 / math.sqrt(D)
+    o, lse = run_bf16(q, k, v, scale, causal)
+    o_ref, lse_ref = attention(q, k, v, scale, causal)
+    check_bf16(o, lse, o_ref, lse_ref, f"bf16 B{B} H{H} M{M} N{N} D{D} causal={causal}")
+
+
+def test_bf16_ragged_cross_workload_all_outputs():
+    """B=2, H=8, M=1000, N=3000, D=96, Q and K ~ N(0, 9): peaked softmax, the
+    running max moves often; every output checked."""
+    w = WORKLOADS["cross_b2_h8_m1000_n3000_d96_peaked"]
+    q, k, v = make_inputs(w)
+    o, lse = run_bf16(q, k, v, w.scale, w.causal)
+    o_ref, lse_ref = attention(q, k, v, w.scale, w.causal)
+    check_bf16(o, lse, o_ref, lse_ref, w.name)
+
+
+def test_bf16_large_logits_many_tiles():
+    """The running max changes in many tiles: a forgotten rescale of the
+    accumulator or of l would be caught here (N spans 16 key tiles)."""
+    q = _rand((1, 2, 256, 64), 41, sigma=3.0)
+    k = _rand((1, 2, 2048, 64), 42, sigma=3.0)
+    v = _rand((1, 2, 2048, 64), 43)
+    # make later tiles hold larger scores so the max keeps rising
+    ramp = np.linspace(0.5, 1.5, 2048, dtype=np.float32)[None, None, :, None]
+    k = round_to_bf16(k * ramp)
+    o, lse = run_bf16(q, k, v, 0.125, False)
+    o_ref, lse_ref = attention(q, k, v, 0.125, False)
+    check_bf16(o, lse, o_ref, lse_ref, "rising max")
+
+
+def test_bf16_worked_example_padded():
+    """The worked example embedded in D = 64 (other features zero): output
+    25.752; the bound is the bf16 rounding of p (2^-9 relative) times |V| = 30
+    plus the output's own half ulp."""
+    q = np.zeros((1, 1, 1, 64), np.float32)
+    q[..., 0] = 1
+    k = np.zeros((1, 1, 3, 64), np.float32)
+    k[0, 0, :, 0] = [1, 2, 3]
+    v = np.zeros((1, 1, 3, 64), np.float32)
+    v[0, 0, :, 0] = [10, 20, 30]
+    o, lse = run_bf16(q, k, v, 1.0, False)
+    assert abs(o[0, 0, 0, 0] - 25.752103826) <= 30 * 2.0 ** -9 + 0.0625
+    assert np.all(o[0, 0, 0, 1:] == 0)
+    assert abs(lse[0, 0, 0] - 3.4076059644) <= 1e-3
+
+
+def test_bf16_empty_keys_and_empty_problem():
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    q = torch.randn(1, 2, 130, 64, device="cuda").to(torch.bfloat16)
+    k = torch.empty(1, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    o = torch.full_like(q, 7.0)
+    lse = torch.zeros(1, 2, 130, device="cuda")
+    fa.fa_fwd(q, k, k, o, lse, 0.125, False)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    q0 = torch.empty(1, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    fa.fa_fwd(q0, q, q, torch.empty_like(q0), torch.empty(1, 2, 0, device="cuda"), 0.125, True)
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
+def test_bf16_deterministic_and_stream():
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q = torch.randn(2, 4, 700, 128, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(2, 4, 900, 128, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(2, 4, 900, 128, device="cuda", generator=g).to(torch.bfloat16)
+    outs = []
+    s = torch.cuda.Stream()
+    for stream in (None, s):
+        o = torch.empty_like(q)
+        lse = torch.empty(2, 4, 700, device="cuda")
+        with torch.cuda.stream(s if stream is not None else torch.cuda.current_stream()):
+            fa.fa_fwd(q, k, v, o, lse, 0.0883883, True)
+        torch.cuda.synchronize()
+        outs.append((o.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+# ------------------------------------------------ full-size workloads (sampled)
+
+def _full_size_check(w, heads, rows_per_head):
+    """Runs the whole workload on the GPU in the benchmark's launch shape and
+    checks sampled heads and rows against the oracle, plus properties of all
+    outputs."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    q, k, v = make_inputs(w)
+    tq, tk, tv = (torch.from_numpy(x).to("cuda").to(torch.bfloat16) for x in (q, k, v))
+    del q, k, v
+    o = torch.empty_like(tq)
+    lse = torch.empty(w.B, w.H, w.M, dtype=torch.float32, device="cuda")
+    fa.fa_fwd(tq, tk, tv, o, lse, w.scale, w.causal)
+    assert fa.fa_get_device_status() == fa.FA_OK
+    # properties over every output: finite, inside the hull of V per feature
+    assert bool(torch.isfinite(o.float()).all()) and bool(torch.isfinite(lse).all())
+    vmax = tv.float().amax(dim=2, keepdim=True)
+    vmin = tv.float().amin(dim=2, keepdim=True)
+    slack = 1e-2
+    assert bool((o.float() <= vmax + slack).all()) and bool((o.float() >= vmin - slack).all())
+    o_np = o.float().cpu().numpy()
+    lse_np = lse.cpu().numpy()
+    for bh in heads:
+        b, h = divmod(bh, w.H)
+        rows = sample_rows(w.wid, bh, w.M, rows_per_head)
+        qh = head_tensor(w.wid, 0, bh, w.M, w.D, w.sigma_qk, w.dtype)
+        kh = head_tensor(w.wid, 1, bh, w.N, w.D, w.sigma_qk, w.dtype)
+        vh = head_tensor(w.wid, 2, bh, w.N, w.D, w.sigma_v, w.dtype)
+        o_ref, lse_ref = attention_rows(qh, kh, vh, w.scale, w.causal, rows)
+        check_bf16(o_np[b, h, rows], lse_np[b, h, rows], o_ref, lse_ref, f"{w.name} head {bh}")
+
+
+def test_full_gpt2_medium_shape():
+    w = WORKLOADS["gpt2m_b64_h16_s1024_d64"]
+    _full_size_check(w, heads=[0, 1, 517, w.B * w.H - 1], rows_per_head=256)
+
+
+def test_full_causal_4k_d128():
+    w = WORKLOADS["causal_b8_h32_s4096_d128"]
+    _full_size_check(w, heads=[0, 37, 130, w.B * w.H - 1], rows_per_head=256)
+
+
+def test_full_long_causal_64k_sampled_rows():
+    """256 seeded rows per head, all 8 heads, against the 64K-key oracle."""
+    w = WORKLOADS["long_causal_b1_h8_s65536_d64"]
+    _full_size_check(w, heads=list(range(w.B * w.H)), rows_per_head=256)
