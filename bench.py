@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU seconds for the oracle sample")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size B (smaller cases for profiler captures)")
     return ap.parse_args(argv)
 
 
@@ -412,6 +414,10 @@ def main(argv=None):
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_batch{args.batch}")
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)

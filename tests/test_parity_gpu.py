@@ -151,6 +151,7 @@ def test_bf16_deterministic_and_stream():
     v = torch.randn(2, 4, 900, 128, device="cuda", generator=g).to(torch.bfloat16)
     outs = []
     s = torch.cuda.Stream()
+    torch.cuda.synchronize()
     for stream in (None, s):
         o = torch.empty_like(q)
         lse = torch.empty(2, 4, 700, device="cuda")
