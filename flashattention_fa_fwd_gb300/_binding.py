@@ -24,7 +24,8 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
-EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error")
+EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
+            "fa_fwd_noalloc")
 
 
 class FaError(RuntimeError):
@@ -54,7 +55,7 @@ def load_library():
                 "(or __graft_entry__.build()) with the CUDA 13 toolkit first")
         lib = ctypes.CDLL(_LIB_PATH)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
-        for name in ("fa_fwd", "fa_fwd_f32"):
+        for name in ("fa_fwd", "fa_fwd_f32", "fa_fwd_noalloc"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
             fn.restype = ctypes.c_int
@@ -80,6 +81,13 @@ def fa_fwd_f32_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: 
                    scale: float, causal: bool, stream: int = 0) -> int:
     """Calls fa_fwd_f32 with raw device addresses; returns the status code."""
     return load_library().fa_fwd_f32(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
+
+
+def fa_fwd_noalloc_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+                       scale: float, causal: bool, stream: int = 0) -> int:
+    """Calls fa_fwd_noalloc (the bf16 forward whose scratch is a static
+    device array, for callers that cannot allocate); returns the status."""
+    return load_library().fa_fwd_noalloc(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
 
 
 def fa_status_string(status: int) -> str:
@@ -165,6 +173,22 @@ def fa_fwd_f32(q, k, v, o, lse, scale: float, causal: bool = False, stream=None)
                             B, H, M, N, D, scale, causal, _stream_of(q, stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_f32")
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, scale: float, causal: bool = False, stream=None) -> None:
+    """bf16 forward like :func:`fa_fwd`, for callers that cannot allocate
+    device memory: the library allocates nothing, not even on the first call
+    (the kernel's scratch is a static device array shared by all calls, so
+    overlapping calls on the GPU race). Make the first call on each device
+    before any stream capture."""
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.bfloat16)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                B, H, M, N, D, scale, causal, _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_noalloc")
 
 
 def fa_get_device_status(stream=None, device=None) -> int:

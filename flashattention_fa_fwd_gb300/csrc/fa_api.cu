@@ -249,3 +249,121 @@ FA_API const char* fa_status_string(int status) {
 }
 
 FA_API const char* fa_last_error(void) { return g_msg; }
+
+// ---------------------------------------------------------------------------
+// fa_fwd_noalloc: the bf16 forward for callers that cannot allocate device
+// memory.
+//
+// fa_fwd keeps its device status word (the kernel's only scratch memory) in
+// a buffer it cudaMallocs on its first call on each device. Some callers
+// cannot allow that: applications whose own caching allocator or memory
+// pool already owns all device memory (a cudaMalloc from a library can fail
+// or defragment their pool), serving loops that must not take the implicit
+// device synchronisation a cudaMalloc/cudaFree can cause, and processes
+// under a fixed device-memory quota. This variant runs the same kernel with
+// its scratch in a file-scope static device array instead, so it never
+// calls cudaMalloc, cudaFree or any allocating routine.
+//
+// The array (kNoAllocScratchWords 32-bit words, 256 bytes) lives on every
+// GPU that loads the library until the process exits. Host code cannot use
+// the array's name as a device address; the first call on each device looks
+// the address up with cudaGetSymbolAddress (with that device current) and
+// caches it, so that first call should come before any stream capture. All
+// calls share the array and it keeps the last call's contents: each call
+// clears the words the kernel expects to start at zero (cudaMemsetAsync on
+// the caller's stream, before the launch), and calls that overlap on the GPU
+// (concurrent streams, or several host threads) race on it.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocScratchWords = 64;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+uint32_t* g_noalloc_scratch_addr[kMaxDevices] = {};
+
+// Words of scratch the bf16 kernel needs: its status word, whatever the
+// problem size.
+constexpr int kBf16ScratchWords = 1;
+
+fa_status noalloc_setup(uint32_t** scratch) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_arch[dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_arch[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch[dev] != 1) return fail(FA_ERR_UNSUPPORTED, "device %d is not sm_103 (this library is built for sm_103a only)", dev);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (g_noalloc_scratch_addr[dev] == nullptr) {
+        uint32_t* ptr = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_scratch_addr[dev] = ptr;
+    }
+    *scratch = g_noalloc_scratch_addr[dev];
+    return FA_OK;
+}
+
+}  // namespace
+
+FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                                int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal,
+                                void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 2, &empty);
+    if (st != FA_OK) return st;
+    if (D != 64 && D != 96 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "bf16 fa_fwd_noalloc supports D in {64, 96, 128} (got %lld)", (long long)D);
+    if (kBf16ScratchWords > kNoAllocScratchWords)
+        return fail(FA_ERR_UNSUPPORTED, "the kernel needs %d scratch words; the static buffer holds %d",
+                    kBf16ScratchWords, kNoAllocScratchWords);
+    if (empty) return FA_OK;
+    const int64_t bh = B * H;
+    const int64_t n_pairs = (M + 255) / 256;
+    if (bh * n_pairs > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many query tiles for one launch");
+    uint32_t* scratch = nullptr;
+    st = noalloc_setup(&scratch);
+    if (st != FA_OK) return st;
+
+    CUtensorMap mq, mk, mv;
+    if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
+    if (N > 0) {
+        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+    } else {
+        mk = mq;
+        mv = mq;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kBf16ScratchWords * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
+    fa::Bf16Params p;
+    p.o = o;
+    p.lse = lse;
+    p.err = scratch;
+    p.bh_count = static_cast<int>(bh);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.n_pairs = static_cast<int>(n_pairs);
+    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    switch (D) {
+        case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
+        case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
+        default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
+    return FA_OK;
+}

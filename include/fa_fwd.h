@@ -115,6 +115,37 @@ fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, f
  */
 fa_status fa_get_device_status(void* stream);
 
+/*
+ * fa_fwd_noalloc: the bf16 forward of fa_fwd (same arguments, layouts,
+ * checks and results) for callers that cannot allocate device memory. The
+ * pages have no counterpart to this entry point; it exists for the library's
+ * users.
+ *
+ * Who needs it: fa_fwd cudaMallocs a 4-byte status word on its first call on
+ * each device. Applications whose caching allocator or memory pool owns all
+ * device memory, serving loops that must avoid the implicit device-wide
+ * synchronisation a cudaMalloc can cause, and processes under a fixed
+ * device-memory quota cannot allow that. This entry point calls no
+ * cudaMalloc, cudaFree or other allocating routine: the kernel's scratch (its
+ * status word) lives in a file-scope static device array of 64 32-bit words
+ * (256 bytes), which every GPU that loads the library holds until the
+ * process exits. No problem size needs more than that one word; a kernel
+ * needing more than the array holds would be rejected with
+ * FA_ERR_UNSUPPORTED.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture. Every call clears the scratch word on
+ * `stream` before its launch. All calls share the one array, so calls that
+ * overlap on the GPU (other streams, other host threads) race on it. A
+ * device-side pipeline timeout in this variant leaves O and LSE undefined
+ * and is not reported by fa_get_device_status(), which reads fa_fwd's own
+ * status word.
+ */
+fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                         float scale, int causal, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(int status);
 
