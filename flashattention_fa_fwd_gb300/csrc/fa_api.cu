@@ -172,6 +172,7 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.n_pairs = static_cast<int>(n_pairs);
+    p.num_units = static_cast<int>(bh * n_pairs);
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -357,6 +358,7 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.n_pairs = static_cast<int>(n_pairs);
+    p.num_units = static_cast<int>(bh * n_pairs);
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     switch (D) {

@@ -1,6 +1,6 @@
 // bf16 FlashAttention forward for sm_103a: TMA-fed shared-memory tiles,
 // tcgen05 MMAs with fp32 accumulators in tensor memory, warp-specialised
-// load / MMA / softmax roles.
+// load / MMA / softmax / correction roles, persistent CTAs.
 //
 // Algorithm ("FlashAttention-style kernel", section "The loop"; "Module 08:
 // FlashAttention and Memory-Efficient Kernels", sections "Tiling and the
@@ -12,15 +12,18 @@
 // score costs one FMA and one base-two exponential. The per-row log-sum-exp
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
-// Work unit: one (batch*head, pair of 128-row query tiles). The two query
-// tiles (t = 0, 1) are processed in ping-pong so that the tensor core works
-// on one tile's matmuls while the other tile's softmax runs.
+// Work unit: one (batch*head, pair of 128-row query tiles). Each CTA is
+// persistent (one per SM) and walks the units u = blockIdx.x, +gridDim.x, ...
+// The two query tiles t = 0, 1 of a unit are processed in ping-pong: while
+// the softmax of one tile runs, the tensor core works on the other tile.
 //
-// Roles (320 threads):
-//   warps 0-3  softmax for query tile 0 (thread = one query row = one TMEM lane)
-//   warps 4-7  softmax for query tile 1
-//   warp  8    TMA producer: Q once, then K_j, V_j into a ring of stages
-//   warp  9    tensor-memory owner and MMA issuer
+// Roles (512 threads, 4 warpgroups; registers re-split with setmaxnreg):
+//   WG0 (warps 0-3)   softmax of query tile 0   (thread = row = TMEM lane)
+//   WG1 (warps 4-7)   softmax of query tile 1
+//   WG2 (warps 8-11)  correction (rescales O by alpha while the softmax
+//                     computes the exponentials) and epilogue (O / l, LSE)
+//   WG3 (warps 12-15) warp 12: TMA producer; warp 13: tensor-memory owner
+//                     and MMA issuer; warps 14-15 idle
 //
 // Tensor memory (512 columns, 128 lanes, lane = query row of the tile):
 //   [  0,128)  S_0 (fp32 scores of tile 0); P_0 (bf16, packed in pairs)
@@ -34,7 +37,18 @@
 // tcgen05 MMAs from one thread execute in issue order, so S_t(j) only
 // overwrites P_t(j-1) after the product that reads it, and the commit that
 // announces S_t(j) also guarantees that O_t holds every earlier product
-// (which is what lets softmax t rescale O_t before releasing P_t(j)).
+// (which is what lets the correction warps rescale O_t before P_t(j) V(j)).
+//
+// Hand-offs per tile j of query tile t (mbarriers):
+//   S_FULL  MMA -> softmax        S_t(j) is in tensor memory
+//   A_FULL  softmax -> correction alpha(j) is in shared memory (sent right
+//                                 after the row max, before the exponentials)
+//   P_FULL  softmax -> MMA        P_t(j) is in tensor memory
+//   O_READY correction -> MMA     O_t has been rescaled by alpha(j)
+// per unit: ST_FULL (softmax -> epilogue: final m, l), O_DONE (MMA ->
+// epilogue: last product done), O_FREE (epilogue -> MMA: O_t may be
+// overwritten by the next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY
+// (TMA ring).
 //
 // Causal (top-left, key j visible to query i when j <= i): key tiles wholly
 // above the diagonal are never loaded or multiplied; the diagonal tile and a
@@ -43,11 +57,16 @@
 // -inf uses 0 in its place so that exp2(-inf - -inf) never forms ("Module
 // 08", "Common mistakes"). Query rows >= M and key rows >= N are zero-filled
 // by TMA, and their scores masked or their outputs not stored.
+//
+// Every wait is bounded (see ptx.cuh): on a time-out the kernel sets the
+// device status word, all roles leave their loops, in-flight copies and
+// MMAs are drained, and tensor memory is freed.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "fa_internal.h"
@@ -63,300 +82,435 @@ struct Bf16Cfg {
     static constexpr int PANELS = (D + 63) / 64;       // 64-column swizzle panels
     static constexpr int PANEL_BYTES = 128 * 128;      // 128 rows x 128 B
     static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-    static constexpr int NS = (D <= 64) ? 8 : 5;       // K/V ring stages
-    static constexpr int NUM_BARS = 2 * NS + 8;
-    static constexpr int SMEM_BYTES = 1024 + (2 + NS) * TILE_BYTES + NUM_BARS * 8;
-    static constexpr int THREADS = 320;
+    static constexpr int QB = (D <= 64) ? 2 : 1;       // Q buffers (units in flight)
+    static constexpr int NS = (D <= 64) ? 8 : 4;       // K/V ring stages
+    static constexpr int THREADS = 512;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 384;
     static constexpr int QK_STEPS = D / 16;            // MMA K-steps of Q K^T
     static constexpr int PV_STEPS = BN / 16;           // MMA K-steps of P V
+    // shared memory layout (offsets from a 1024-byte aligned base)
+    static constexpr int Q_OFF = 0;
+    static constexpr int KV_OFF = Q_OFF + QB * 2 * TILE_BYTES;
+    static constexpr int ALPHA_OFF = KV_OFF + NS * TILE_BYTES;      // float [2][128]
+    static constexpr int STATS_OFF = ALPHA_OFF + 2 * 128 * 4;       // float [2 buf][2 t][2][128]
+    static constexpr int BAR_OFF = STATS_OFF + 2 * 2 * 2 * 128 * 4;
+    // barrier slots
+    static constexpr int KV_FULL = 0, KV_EMPTY = NS, Q_FULL = 2 * NS, Q_EMPTY = 2 * NS + QB;
+    static constexpr int S_FULL = 2 * NS + 2 * QB, P_FULL = S_FULL + 2, A_FULL = S_FULL + 4;
+    static constexpr int O_READY = S_FULL + 6, O_DONE = S_FULL + 8, O_FREE = S_FULL + 10;
+    static constexpr int ST_FULL = S_FULL + 12, DRAIN = S_FULL + 14;
+    static constexpr int NUM_BARS = DRAIN + 1;
+    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Barrier slots in shared memory.
-template <int NS>
-struct Bars {
-    static constexpr int full = 0;            // [NS] K/V stage loaded
-    static constexpr int empty = NS;          // [NS] K/V stage released
-    static constexpr int q_full = 2 * NS;     // Q tiles loaded
-    static constexpr int s_full = 2 * NS + 1; // [2] S_t ready in TMEM
-    static constexpr int p_ready = 2 * NS + 3;// [2] P_t stored and O_t rescaled
-    static constexpr int o_done = 2 * NS + 5; // [2] last P V of tile t complete
-    static constexpr int drain = 2 * NS + 7;  // all MMAs complete (exit)
+// Register split per warpgroup (setmaxnreg); sums to 512 x 128, the launch's
+// registers, and to 512 per SM sub-partition (one warp of each group).
+constexpr int kRegsSoftmax = 176, kRegsCorrection = 64, kRegsLoadMma = 96;
+static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma == 4 * 128, "register split");
+
+struct Unit {
+    int bh, q0, n0, n1, nmax;
 };
 
-__device__ __forceinline__ void decode_unit(int u, int bh_count, int n_pairs, int heads_per_group,
-                                            bool causal, int& bh, int& pair) {
-    if (causal) {
+template <bool CAUSAL>
+__device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
+    Unit U;
+    int pair;
+    if (CAUSAL) {
         // Heads in groups of heads_per_group; inside a group the longest
         // query tiles (largest pair index) come first.
-        const int group_units = heads_per_group * n_pairs;
+        const int group_units = p.heads_per_group * p.n_pairs;
         const int g = u / group_units;
         const int r = u - g * group_units;
-        const int hg = min(heads_per_group, bh_count - g * heads_per_group);
-        pair = n_pairs - 1 - r / hg;
-        bh = g * heads_per_group + r % hg;
+        const int hg = min(p.heads_per_group, p.bh_count - g * p.heads_per_group);
+        pair = p.n_pairs - 1 - r / hg;
+        U.bh = g * p.heads_per_group + r % hg;
     } else {
-        bh = u / n_pairs;
-        pair = u - bh * n_pairs;
+        U.bh = u / p.n_pairs;
+        pair = u - U.bh * p.n_pairs;
+    }
+    U.q0 = pair * 256;
+    const int nkv = (p.N + 127) / 128;
+    // Key tiles each query tile visits (0 when the tile lies beyond M).
+    U.n0 = (U.q0 >= p.M) ? 0 : (CAUSAL ? min(nkv, U.q0 / 128 + 1) : nkv);
+    U.n1 = (U.q0 + 128 >= p.M) ? 0 : (CAUSAL ? min(nkv, (U.q0 + 128) / 128 + 1) : nkv);
+    U.nmax = max(U.n0, U.n1);
+    return U;
+}
+
+struct Ctx {
+    uint32_t bar0;        // shared address of barrier 0
+    uint8_t* sQ;
+    uint8_t* sKV;
+    float* alpha_sm;      // [2][128]
+    float* stats_sm;      // [2 buf][2 t][2 (m, l)][128]
+    uint32_t tmem;
+    volatile int* abort;
+    uint32_t* err;
+    __device__ __forceinline__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
+    __device__ __forceinline__ bool wait(int i, int parity) const {
+        return mbar_wait(bar(i), static_cast<uint32_t>(parity) & 1u, abort, err);
+    }
+    // Whole-warp wait: every lane polls, and all agree on the outcome.
+    __device__ __forceinline__ bool wait_warp(int i, int parity) const {
+        return __all_sync(0xffffffffu, wait(i, parity));
+    }
+    // Per-thread arrive (the hand-off barriers count the 128 threads of a
+    // warpgroup).
+    __device__ __forceinline__ void arrive_warp(int i) const { mbar_arrive(bar(i)); }
+};
+
+// ----------------------------------------------------------- TMA producer
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUtensorMap* mk, const CUtensorMap* mv,
+                                              const Bf16Params& p, const Ctx& c) {
+    using C = Bf16Cfg<D>;
+    const uint64_t pol_q = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_last();
+    int kv_idx = 0, qit = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit U = unit_info<CAUSAL>(u, p);
+        if (U.nmax == 0) continue;
+        const int qb = qit % C::QB;
+        if (qit >= C::QB && !c.wait(C::Q_EMPTY + qb, qit / C::QB - 1)) {
+            ok = false;
+            break;
+        }
+        const int nq = (U.n0 > 0 ? 1 : 0) + (U.n1 > 0 ? 1 : 0);
+        mbar_arrive_expect_tx(c.bar(C::Q_FULL + qb), nq * C::TILE_BYTES);
+        for (int t = 0; t < 2; ++t) {
+            if ((t ? U.n1 : U.n0) == 0) continue;
+            for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_3d(smem_u32(c.sQ + (qb * 2 + t) * C::TILE_BYTES + pn * C::PANEL_BYTES), mq,
+                            c.bar(C::Q_FULL + qb), pn * 64, U.q0 + 128 * t, U.bh, pol_q);
+        }
+        ++qit;
+        for (int j = 0; j < U.nmax && ok; ++j) {
+            for (int which = 0; which < 2; ++which) {
+                const int stage = kv_idx % C::NS;
+                const int round = kv_idx / C::NS;
+                if (round > 0 && !c.wait(C::KV_EMPTY + stage, round - 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(c.bar(C::KV_FULL + stage), C::TILE_BYTES);
+                const CUtensorMap* m = which ? mv : mk;
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_3d(smem_u32(c.sKV + stage * C::TILE_BYTES + pn * C::PANEL_BYTES), m,
+                                c.bar(C::KV_FULL + stage), pn * 64, j * C::BN, U.bh, pol_kv);
+                ++kv_idx;
+            }
+        }
+    }
+    // Every copy issued must land before this CTA's shared memory is
+    // released: wait for the last fill of each stage and of each Q buffer.
+    for (int s = 0; s < C::NS && s < kv_idx; ++s) {
+        const int last = s + ((kv_idx - 1 - s) / C::NS) * C::NS;
+        mbar_wait_drain(c.bar(C::KV_FULL + s), (last / C::NS) & 1);
+    }
+    for (int b = 0; b < C::QB && b < qit; ++b) {
+        const int last = b + ((qit - 1 - b) / C::QB) * C::QB;
+        mbar_wait_drain(c.bar(C::Q_FULL + b), (last / C::QB) & 1);
     }
 }
 
+// ------------------------------------------------------------- MMA issuer
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(Bf16Cfg<D>::THREADS, 1)
-fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                   const __grid_constant__ CUtensorMap map_v, const Bf16Params p) {
+__device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
     using C = Bf16Cfg<D>;
-    using B = Bars<C::NS>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;                                  // 2 tiles
-    uint8_t* sKV = smem + 2 * C::TILE_BYTES;             // NS tiles
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::NS * C::TILE_BYTES);
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int abort_sh;
+    constexpr uint32_t id_s = idesc_bf16_f32(128, C::BN, false);
+    constexpr uint32_t id_o = idesc_bf16_f32(128, D, true);
+    const uint32_t sq = smem_u32(c.sQ);
+    const uint32_t skv = smem_u32(c.sKV);
+    // Descriptor templates with a zero start address; adding (address >> 4)
+    // fills the 14-bit start field (shared addresses are < 256 KB).
+    const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);
+    const uint64_t desc_v = smem_desc_sw128(0, C::PANEL_BYTES, 1024);
+    int kv_idx = 0, qit = 0;
+    int pv_cnt[2] = {0, 0};   // P V products issued per query tile
+    int units_o[2] = {0, 0};  // units whose last product was committed, per tile
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit U = unit_info<CAUSAL>(u, p);
+        if (U.nmax == 0) continue;
+        const int qb = qit % C::QB;
+        if (!c.wait(C::Q_FULL + qb, qit / C::QB)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        for (int j = 0; j <= U.nmax && ok; ++j) {
+            const int kidx = kv_idx + 2 * j, vidx = kv_idx + 2 * j - 1;
+            const int kst = kidx % C::NS, vst = (vidx + C::NS) % C::NS;
+            // V(j-1) gates the P V products, K(j) only the Q K^T ones.
+            if (j >= 1 && !c.wait(C::KV_FULL + vst, vidx / C::NS)) ok = false;
+            bool k_ready = false;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int nt = t ? U.n1 : U.n0;
+                const uint32_t s_col = t ? C::S_COL1 : C::S_COL0;
+                const uint32_t o_col = t ? C::O_COL1 : C::O_COL0;
+                if (ok && j >= 1 && j - 1 < nt) {
+                    ok = c.wait(C::P_FULL + t, pv_cnt[t]) && c.wait(C::O_READY + t, pv_cnt[t]);
+                    // The first product of a unit overwrites O_t: the
+                    // previous unit's epilogue must have read it.
+                    if (ok && j == 1 && units_o[t] > 0) ok = c.wait(C::O_FREE + t, units_o[t] - 1);
+                    if (ok) {
+                        tc_fence_after();
+                        // V tile: MN-major, 128-byte swizzle; LBO = the
+                        // 64-column panel stride, SBO = 8 rows of 128 B.
+                        const uint64_t dv = desc_v + ((skv + vst * C::TILE_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                            mma_ts(c.tmem + o_col, c.tmem + s_col + kk * 8, dv + kk * (2048 >> 4), id_o,
+                                   (j > 1 || kk > 0) ? 1u : 0u);
+                        ++pv_cnt[t];
+                        if (j == nt) {
+                            mma_commit(c.bar(C::O_DONE + t));
+                            ++units_o[t];
+                        }
+                        // V(j-1) is free once its last product completes
+                        // (a commit covers every MMA issued before it).
+                        // Tile 1 is issued after tile 0, so it is V's last
+                        // user whenever it uses V(j-1) at all.
+                        if (t == 1 || j - 1 >= U.n1) mma_commit(c.bar(C::KV_EMPTY + vst));
+                    }
+                }
+                if (ok && j < nt && !k_ready) {
+                    ok = c.wait(C::KV_FULL + kst, kidx / C::NS);
+                    k_ready = ok;
+                    tc_fence_after();
+                }
+                if (ok && j < nt) {
+                    // Q and K tiles: K-major, 128-byte swizzle; a 16-column
+                    // K-step advances 32 B inside a panel, 4 steps a panel.
+                    const uint64_t dq = desc_k + ((sq + (qb * 2 + t) * C::TILE_BYTES) >> 4);
+                    const uint64_t dk = desc_k + ((skv + kst * C::TILE_BYTES) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                        constexpr uint32_t kPanel = C::PANEL_BYTES >> 4;
+                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+                        mma_ss(c.tmem + s_col, dq + off, dk + off, id_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(c.bar(C::S_FULL + t));
+                }
+            }
+            if (!ok) break;
+            if (j < U.nmax) mma_commit(c.bar(C::KV_EMPTY + kst));
+            if (j == U.nmax - 1) mma_commit(c.bar(C::Q_EMPTY + qb));
+        }
+        kv_idx += 2 * U.nmax;
+        ++qit;
+    }
+    // All MMAs issued must finish before tensor memory is freed.
+    mma_commit(c.bar(C::DRAIN));
+    mbar_wait_drain(c.bar(C::DRAIN), 0);
+}
 
+// ---------------------------------------------------------------- softmax
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const Ctx& c) {
+    using C = Bf16Cfg<D>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    volatile int* abort_flag = &abort_sh;
-    auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
-
-    int bh, pair;
-    decode_unit(blockIdx.x, p.bh_count, p.n_pairs, p.heads_per_group, CAUSAL, bh, pair);
-    const int q0 = pair * 256;
-    const int nkv = (p.N + C::BN - 1) / C::BN;
-    int n_t[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int qs = q0 + 128 * t;
-        if (qs >= p.M) n_t[t] = 0;
-        else n_t[t] = CAUSAL ? min(nkv, qs / C::BN + 1) : nkv;
-    }
-    const int nmax = max(n_t[0], n_t[1]);
-
-    if (threadIdx.x == 0) {
-        abort_sh = 0;
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(bar(B::full + s), 1);
-            mbar_init(bar(B::empty + s), 1);
-        }
-        mbar_init(bar(B::q_full), 1);
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(B::s_full + t), 1);
-            mbar_init(bar(B::p_ready + t), 128);
-            mbar_init(bar(B::o_done + t), 1);
-        }
-        mbar_init(bar(B::drain), 1);
-        fence_barrier_init();
-    }
-    if (warp == 9) {
-        tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    if (warp == 8 && lane == 0) {
-        tma_prefetch_desc(&map_q);
-        tma_prefetch_desc(&map_k);
-        tma_prefetch_desc(&map_v);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_sh;
-
-    if (warp == 8) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_q = policy_evict_first();
-            const uint64_t pol_kv = policy_evict_last();
-            const int nq = (n_t[0] > 0 ? 1 : 0) + (n_t[1] > 0 ? 1 : 0);
-            if (nq > 0) {
-                mbar_arrive_expect_tx(bar(B::q_full), nq * C::TILE_BYTES);
-                for (int t = 0; t < 2; ++t) {
-                    if (n_t[t] == 0) continue;
-                    for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(smem_u32(sQ + t * C::TILE_BYTES + pn * C::PANEL_BYTES), &map_q,
-                                    bar(B::q_full), pn * 64, q0 + 128 * t, bh, pol_q);
-                }
-            }
-            int idx = 0;
-            bool ok = true;
-            for (int j = 0; j < nmax && ok; ++j) {
-                for (int which = 0; which < 2; ++which) {
-                    const int stage = idx % C::NS;
-                    const int round = idx / C::NS;
-                    if (round > 0 && !mbar_wait(bar(B::empty + stage), (round - 1) & 1, abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(B::full + stage), C::TILE_BYTES);
-                    const CUtensorMap* m = which ? &map_v : &map_k;
-                    for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_3d(smem_u32(sKV + stage * C::TILE_BYTES + pn * C::PANEL_BYTES), m,
-                                    bar(B::full + stage), pn * 64, j * C::BN, bh, pol_kv);
-                    ++idx;
-                }
-            }
-            // Every copy issued must land before this CTA's shared memory is
-            // released: wait for the last fill of each stage and for Q.
-            for (int s = 0; s < C::NS && s < idx; ++s) {
-                const int last = s + ((idx - 1 - s) / C::NS) * C::NS;
-                mbar_wait_drain(bar(B::full + s), (last / C::NS) & 1);
-            }
-            if (nq > 0) mbar_wait_drain(bar(B::q_full), 0);
-        }
-        __syncwarp();
-    } else if (warp == 9) {
-        // ----------------------------------------------------- MMA issuer
-        if (lane == 0 && nmax > 0) {
-            constexpr uint32_t id_s = idesc_bf16_f32(128, C::BN, false);
-            constexpr uint32_t id_o = idesc_bf16_f32(128, D, true);
-            const uint32_t sq = smem_u32(sQ);
-            const uint32_t skv = smem_u32(sKV);
-            const uint32_t s_col[2] = {C::S_COL0, C::S_COL1};
-            const uint32_t o_col[2] = {C::O_COL0, C::O_COL1};
-            bool ok = mbar_wait(bar(B::q_full), 0, abort_flag, p.err);
-            tc_fence_after();
-            for (int j = 0; j <= nmax && ok; ++j) {
-                const int kidx = 2 * j, vidx = 2 * j - 1;
-                const int kst = kidx % C::NS, vst = (vidx + C::NS) % C::NS;
-                if (j < nmax && !mbar_wait(bar(B::full + kst), (kidx / C::NS) & 1, abort_flag, p.err)) break;
-                if (j >= 1 && !mbar_wait(bar(B::full + vst), (vidx / C::NS) & 1, abort_flag, p.err)) break;
-                tc_fence_after();
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= 1 && j - 1 < n_t[t]) {
-                        if (!mbar_wait(bar(B::p_ready + t), (j - 1) & 1, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t vb = skv + vst * C::TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-                            const uint64_t bd = smem_desc_sw128(vb + kk * 2048, C::PANEL_BYTES, 1024);
-                            mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, bd, id_o,
-                                   (j > 1 || kk > 0) ? 1u : 0u);
-                        }
-                        if (j - 1 == n_t[t] - 1) mma_commit(bar(B::o_done + t));
-                    }
-                    if (j < n_t[t]) {
-                        const uint32_t qb = sq + t * C::TILE_BYTES;
-                        const uint32_t kb = skv + kst * C::TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                            const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                            const uint64_t ad = smem_desc_sw128(qb + off, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(kb + off, 16, 1024);
-                            mma_ss(tmem + s_col[t], ad, bd, id_s, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar(B::s_full + t));
-                    }
-                }
-                if (!ok) break;
-                if (j < nmax) mma_commit(bar(B::empty + kst));
-                if (j >= 1) mma_commit(bar(B::empty + vst));
-            }
-            // All MMAs issued must finish before tensor memory is freed.
-            mma_commit(bar(B::drain));
-            mbar_wait_drain(bar(B::drain), 0);
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------------- softmax
-        const int t = warp >> 2;
-        const int wq = warp & 3;
-        const int r = wq * 32 + lane;                       // row in the tile
-        const int qrow = q0 + 128 * t + r;                  // query row
-        const int ntile = n_t[t];
-        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + (t ? C::S_COL1 : C::S_COL0);
-        const uint32_t o_addr = tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
-        const float c = p.scale_log2;
+    const int r = (warp & 3) * 32 + lane;                   // row in the tile = TMEM lane
+    const uint32_t s_addr = c.tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (t ? C::S_COL1 : C::S_COL0);
+    const float cl2 = p.scale_log2;
+    const uint64_t c2 = f2_pack(cl2, cl2);
+    int s_cnt = 0, st_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit U = unit_info<CAUSAL>(u, p);
+        const int ntile = t ? U.n1 : U.n0;
+        if (ntile == 0) continue;
+        const int qt0 = U.q0 + 128 * t;                     // first row of the tile
+        const int qrow = qt0 + r;
         float m_run = -INFINITY;   // running max of scaled scores, base-2 units
         float l_run = 0.f;         // running sum of exp2(score - m_run)
-        bool ok = true;
-
         for (int j = 0; j < ntile; ++j) {
             // Every lane must agree: the tensor-memory loads below are
             // warp-collective.
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(B::s_full + t), j & 1, abort_flag, p.err))) {
+            if (!c.wait_warp(C::S_FULL + t, s_cnt)) {
                 ok = false;
                 break;
             }
+            ++s_cnt;
             tc_fence_after();
             uint32_t s[128];
-            {
-                uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-                uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-                uint32_t (&cc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
-                uint32_t (&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
-                tmem_ld_x32(s_addr + 0, a);
-                tmem_ld_x32(s_addr + 32, b);
-                tmem_ld_x32(s_addr + 64, cc);
-                tmem_ld_x32(s_addr + 96, d);
-                tmem_ld_wait(s);
-            }
+            uint32_t (&s_lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[0]);
+            uint32_t (&s_hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[64]);
+            tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            tmem_ld_wait(s_lo);
+            // The second half is in flight while the first half is reduced.
+            tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+            tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
             const int kv0 = j * C::BN;
-            const bool need_mask = (kv0 + C::BN > p.N) || (CAUSAL && kv0 + C::BN - 1 > q0 + 128 * t);
+            const bool need_mask = (kv0 + C::BN > p.N) || (CAUSAL && kv0 + C::BN - 1 > qt0);
+            int lim = 128;
             if (need_mask) {
-                int lim = p.N - kv0;                         // key columns < N
+                lim = p.N - kv0;                             // key columns < N
                 if (CAUSAL) lim = min(lim, qrow - kv0 + 1);  // key <= query
 #pragma unroll
-                for (int i = 0; i < 128; ++i)
+                for (int i = 0; i < 64; ++i)
                     if (i >= lim) s[i] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(s[0]);
+            // Row max: four independent chains of three-input maxima.
+            float mx0 = fmaxf(__uint_as_float(s[0]), __uint_as_float(s[1]));
+            float mx1 = fmaxf(__uint_as_float(s[2]), __uint_as_float(s[3]));
+            float mx2 = fmaxf(__uint_as_float(s[4]), __uint_as_float(s[5]));
+            float mx3 = fmaxf(__uint_as_float(s[6]), __uint_as_float(s[7]));
 #pragma unroll
-            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
-            const float m_new = fmaxf(m_run, mx * c);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = ex2(m_run - m_use);
-            const float neg = -m_use;
-            float sum0 = 0.f, sum1 = 0.f;
+            for (int i = 8; i < 64; i += 8) {           // s[8..63]: the loaded half only
+                mx0 = fmax3(mx0, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+            }
+            tmem_ld_wait(s_hi);
+            if (need_mask) {
+#pragma unroll
+                for (int i = 64; i < 128; ++i)
+                    if (i >= lim) s[i] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int i = 64; i < 128; i += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+            }
+            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            // New running max; alpha rescales what was accumulated so far
+            // (1 for rows whose max did not move). It goes to the correction
+            // warps now, so that the rescale of O overlaps the exponentials.
+            const float m_tile = mx * cl2;                   // -inf if all masked
+            const bool grow = m_tile > m_run;                // first visible tile: m_run = -inf
+            const float m_new = grow ? m_tile : m_run;
+            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // no -inf - -inf
+            c.alpha_sm[t * 128 + r] = alpha;
+            c.arrive_warp(C::A_FULL + t);
+            const uint64_t neg2 = f2_pack(-m_use, -m_use);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), c, neg));
-                const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), c, neg));
-                sum0 += p0;
-                sum1 += p1;
+                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), c2, neg2);
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                const float p0 = ex2(x0);
+                const float p1 = ex2(x1);
+                acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(p0, p1));
                 pk[i] = pack_bf16x2(p0, p1);
             }
-            l_run = l_run * alpha + (sum0 + sum1);
-            m_run = m_new;
             tmem_st_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
             tmem_st_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-            // Rescale the output accumulator to the new max (tile 0 has no
-            // accumulator yet: its first product overwrites O).
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t ov[32];
-                    tmem_ld_x32(o_addr + cc * 32, ov);
-                    tmem_ld_wait(ov);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st_x32(o_addr + cc * 32, ov);
-                }
-            }
+            float sa, sb, sc, sd;
+            f2_unpack(f2_add(acc2[0], acc2[1]), sa, sb);
+            f2_unpack(f2_add(acc2[2], acc2[3]), sc, sd);
+            l_run = l_run * alpha + ((sa + sb) + (sc + sd));
+            m_run = m_new;
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(B::p_ready + t));
+            c.arrive_warp(C::P_FULL + t);
         }
+        if (!ok) break;
+        // Final statistics of this tile for the epilogue (double-buffered by
+        // unit, so the next unit's values never overwrite unread ones).
+        float* st = c.stats_sm + ((st_cnt & 1) * 2 + t) * 256;
+        st[r] = m_run;
+        st[128 + r] = l_run;
+        c.arrive_warp(C::ST_FULL + t);
+        ++st_cnt;
+    }
+}
 
-        // ---------------------------------------------------------- epilogue
-        if (ok && ntile > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B::o_done + t), 0, abort_flag, p.err));
-            tc_fence_after();
+// ------------------------------------------------ correction and epilogue
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void correction_role(const Bf16Params& p, const Ctx& c) {
+    using C = Bf16Cfg<D>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int a_cnt[2] = {0, 0}, st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit U = unit_info<CAUSAL>(u, p);
+        for (int j = 0; j < U.nmax && ok; ++j) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!ok || j >= (t ? U.n1 : U.n0)) continue;
+                if (!c.wait_warp(C::A_FULL + t, a_cnt[t])) {
+                    ok = false;
+                    break;
+                }
+                ++a_cnt[t];
+                if (j > 0) {
+                    const float alpha = c.alpha_sm[t * 128 + r];
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                        tc_fence_after();
+                        const uint32_t o_addr = c.tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
+                        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t ov[32];
+                            tmem_ld_x32(o_addr + cc * 32, ov);
+                            tmem_ld_wait(ov);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint64_t v2 = f2_fma(f2_pack(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])),
+                                                           a2, 0ull);
+                                float lo, hi;
+                                f2_unpack(v2, lo, hi);
+                                ov[2 * i] = __float_as_uint(lo);
+                                ov[2 * i + 1] = __float_as_uint(hi);
+                            }
+                            tmem_st_x32(o_addr + cc * 32, ov);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                tc_fence_before();
+                c.arrive_warp(C::O_READY + t);
+            }
         }
-        if (ok && q0 + 128 * t < p.M) {
-            const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        if (!ok) break;
+        // Epilogue: O = acc / l in bf16, LSE = ln2 * (m + log2 l).
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int nt = t ? U.n1 : U.n0;
+            const int qt0 = U.q0 + 128 * t;
+            if (!ok || qt0 >= p.M) continue;
+            float m_fin = -INFINITY, l_fin = 0.f;
+            if (nt > 0) {
+                bool w = c.wait_warp(C::ST_FULL + t, st_cnt[t]);
+                w = w && c.wait_warp(C::O_DONE + t, od_cnt[t]);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                const float* st = c.stats_sm + ((st_cnt[t] & 1) * 2 + t) * 256;
+                m_fin = st[r];
+                l_fin = st[128 + r];
+                ++st_cnt[t];
+                ++od_cnt[t];
+                tc_fence_after();
+            }
+            const int qrow = qt0 + r;
             const bool store = qrow < p.M;
+            const float inv_l = (l_fin > 0.f) ? 1.f / l_fin : 0.f;
+            const uint32_t o_addr = c.tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
             uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +   // bf16 bits
-                             (static_cast<size_t>(bh) * p.M + (store ? qrow : 0)) * D;
+                             (static_cast<size_t>(U.bh) * p.M + (store ? qrow : 0)) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t ov[32];
-                if (ntile > 0) {
+                if (nt > 0) {
                     tmem_ld_x32(o_addr + cc * 32, ov);
                     tmem_ld_wait(ov);
                 } else {
@@ -374,31 +528,123 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
                         dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
                 }
             }
-            if (store) {
-                // LSE in natural-log units: ln2 * (m + log2 l); -inf when no key was visible.
-                p.lse[static_cast<size_t>(bh) * p.M + qrow] =
-                    (l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            if (store)
+                p.lse[static_cast<size_t>(U.bh) * p.M + qrow] =
+                    (l_fin > 0.f) ? (m_fin + log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
+            if (nt > 0) {
+                tc_fence_before();
+                c.arrive_warp(C::O_FREE + t);
             }
+        }
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Bf16Cfg<D>::THREADS, 1)
+fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const __grid_constant__ CUtensorMap map_v, const Bf16Params p) {
+    using C = Bf16Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    Ctx c;
+    c.bar0 = smem_u32(smem + C::BAR_OFF);
+    c.sQ = smem + C::Q_OFF;
+    c.sKV = smem + C::KV_OFF;
+    c.alpha_sm = reinterpret_cast<float*>(smem + C::ALPHA_OFF);
+    c.stats_sm = reinterpret_cast<float*>(smem + C::STATS_OFF);
+    c.abort = &abort_sh;
+    c.err = p.err;
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(c.bar(C::KV_FULL + s), 1);
+            mbar_init(c.bar(C::KV_EMPTY + s), 1);
+        }
+        for (int b = 0; b < C::QB; ++b) {
+            mbar_init(c.bar(C::Q_FULL + b), 1);
+            mbar_init(c.bar(C::Q_EMPTY + b), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(c.bar(C::S_FULL + t), 1);
+            mbar_init(c.bar(C::P_FULL + t), 128);
+            mbar_init(c.bar(C::A_FULL + t), 128);
+            mbar_init(c.bar(C::O_READY + t), 128);
+            mbar_init(c.bar(C::O_DONE + t), 1);
+            mbar_init(c.bar(C::O_FREE + t), 128);
+            mbar_init(c.bar(C::ST_FULL + t), 128);
+        }
+        mbar_init(c.bar(C::DRAIN), 1);
+        fence_barrier_init();
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem = tmem_base_sh;
+
+    const int wg = warp >> 2;
+    if (wg < 2) {
+        setmaxnreg_inc<kRegsSoftmax>();
+        softmax_role<D, CAUSAL>(wg, p, c);
+    } else if (wg == 2) {
+        setmaxnreg_dec<kRegsCorrection>();
+        correction_role<D, CAUSAL>(p, c);
+    } else {
+        setmaxnreg_dec<kRegsLoadMma>();
+        if (warp == 12) {
+            if (lane == 0) producer_role<D, CAUSAL>(&map_q, &map_k, &map_v, p, c);
+            __syncwarp();
+        } else if (warp == 13) {
+            if (lane == 0) mma_role<D, CAUSAL>(p, c);
+            __syncwarp();
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc(c.tmem, C::TMEM_COLS);
     }
+}
+
+inline int sm_count_cached() {
+    static std::atomic<int> counts[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 template <int D>
 cudaError_t launch_bf16(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Bf16Params& p,
                         bool causal, cudaStream_t stream) {
     using C = Bf16Cfg<D>;
-    const int units = p.bh_count * p.n_pairs;
+    const int sms = sm_count_cached();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = p.num_units < sms ? p.num_units : sms;   // persistent: one CTA per SM
     auto kern = causal ? fa_fwd_bf16_kernel<D, true> : fa_fwd_bf16_kernel<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<units, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 

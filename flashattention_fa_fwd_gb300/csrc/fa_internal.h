@@ -20,6 +20,7 @@ struct Bf16Params {
     int M;
     int N;
     int n_pairs;         // ceil(M / 256): units of two 128-row query tiles
+    int num_units;       // bh_count * n_pairs
     int heads_per_group; // causal tile order: heads that share a group
     float scale_log2;    // scale * log2(e)
 };
