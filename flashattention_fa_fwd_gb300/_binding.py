@@ -25,7 +25,7 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
-            "fa_fwd_noalloc")
+            "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest")
 
 
 class FaError(RuntimeError):
@@ -59,6 +59,13 @@ def load_library():
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
             fn.restype = ctypes.c_int
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                        ctypes.c_int, vp, i64, vp]
+        lib.fa_fwd_splitkv.restype = ctypes.c_int
+        lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+        lib.fa_fwd_splitkv_workspace_bytes.restype = i64
+        lib.fa_fwd_splitkv_suggest.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+        lib.fa_fwd_splitkv_suggest.restype = ctypes.c_int
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = ctypes.c_int
         lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -88,6 +95,22 @@ def fa_fwd_noalloc_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int,
     """Calls fa_fwd_noalloc (the bf16 forward whose scratch is a static
     device array, for callers that cannot allocate); returns the status."""
     return load_library().fa_fwd_noalloc(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
+
+
+def fa_fwd_splitkv_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+                       scale: float, causal: bool, num_splits: int, workspace: int, workspace_bytes: int,
+                       stream: int = 0) -> int:
+    """Calls fa_fwd_splitkv with raw device addresses; returns the status."""
+    return load_library().fa_fwd_splitkv(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)),
+                                         int(num_splits), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, M: int, D: int, num_splits: int) -> int:
+    return load_library().fa_fwd_splitkv_workspace_bytes(B, H, M, D, num_splits)
+
+
+def fa_fwd_splitkv_suggest(B: int, H: int, M: int, N: int, causal: bool) -> int:
+    return load_library().fa_fwd_splitkv_suggest(B, H, M, N, int(bool(causal)))
 
 
 def fa_status_string(status: int) -> str:
@@ -173,6 +196,28 @@ def fa_fwd_f32(q, k, v, o, lse, scale: float, causal: bool = False, stream=None)
                             B, H, M, N, D, scale, causal, _stream_of(q, stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_f32")
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, scale: float, causal: bool = False, num_splits: int = 0,
+                   workspace=None, stream=None) -> None:
+    """Split-KV bf16 forward (same result as :func:`fa_fwd`). ``num_splits``
+    0 asks the library for a split count; ``workspace`` is a CUDA tensor of at
+    least fa_fwd_splitkv_workspace_bytes(...) bytes (allocated here with torch
+    when None)."""
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.bfloat16)
+    with torch.cuda.device(q.device):
+        if num_splits == 0:
+            num_splits = fa_fwd_splitkv_suggest(B, H, M, N, causal)
+        need = fa_fwd_splitkv_workspace_bytes(B, H, M, D, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                B, H, M, N, D, scale, causal, num_splits, workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_splitkv")
 
 
 def fa_fwd_noalloc(q, k, v, o, lse, scale: float, causal: bool = False, stream=None) -> None:

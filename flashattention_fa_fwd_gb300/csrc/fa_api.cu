@@ -172,7 +172,10 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.n_pairs = static_cast<int>(n_pairs);
+    p.splits = 1;
     p.num_units = static_cast<int>(bh * n_pairs);
+    p.ws_o = nullptr;
+    p.ws_lse = nullptr;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -250,6 +253,103 @@ FA_API const char* fa_status_string(int status) {
 }
 
 FA_API const char* fa_last_error(void) { return g_msg; }
+
+// ---------------------------------------------------------------------------
+// Split-KV: each query tile's keys are cut into `num_splits` contiguous ranges
+// processed by different CTAs, which write partial results into a caller-
+// provided workspace; a merge kernel combines them. Worth it when B*H*M is
+// too small to fill the GPU (few query tiles, long keys).
+// ---------------------------------------------------------------------------
+namespace {
+
+int64_t splitkv_bytes(int64_t bh, int64_t M, int64_t D, int64_t splits) {
+    return splits * bh * M * (D + 1) * static_cast<int64_t>(sizeof(float));
+}
+
+}  // namespace
+
+FA_API int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t D, int num_splits) {
+    if (B < 0 || H < 0 || M < 0 || D < 1 || num_splits < 1) return -1;
+    if (num_splits == 1) return 0;
+    return splitkv_bytes(B * H, M, D, num_splits);
+}
+
+FA_API int fa_fwd_splitkv_suggest(int64_t B, int64_t H, int64_t M, int64_t N, int causal) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    const int64_t units = B * H * ((M + 255) / 256);
+    const int64_t nkv = (N + 127) / 128;
+    if (units <= 0 || nkv < 4 || causal) return 1;
+    int64_t s = sms / units;                 // fill the SMs once, no more
+    if (s > nkv / 2) s = nkv / 2;            // at least two key tiles per split
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : static_cast<int>(s);
+}
+
+FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                                int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal, int num_splits,
+                                void* workspace, int64_t workspace_bytes, void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 2, &empty);
+    if (st != FA_OK) return st;
+    if (D != 64 && D != 96 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "bf16 fa_fwd_splitkv supports D in {64, 96, 128} (got %lld)", (long long)D);
+    if (num_splits < 1 || num_splits > 16)
+        return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, 16] (got %d)", num_splits);
+    if (num_splits == 1) return fa_fwd(q, k, v, o, lse, B, H, M, N, D, scale, causal, stream);
+    const int64_t bh = B * H;
+    const int64_t need = splitkv_bytes(bh, M, D, num_splits);
+    if (empty) return FA_OK;
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(FA_ERR_INVALID_ARG, "workspace of %lld bytes needed (got %lld)", (long long)need,
+                    (long long)workspace_bytes);
+    if (!aligned(workspace, 16)) return fail(FA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const int64_t qbytes = bh * M * D * 2, kvbytes = bh * N * D * 2;
+    if (overlaps(workspace, need, q, qbytes) || overlaps(workspace, need, k, kvbytes) ||
+        overlaps(workspace, need, v, kvbytes) || overlaps(workspace, need, o, qbytes) ||
+        overlaps(workspace, need, lse, bh * M * 4))
+        return fail(FA_ERR_INVALID_ARG, "workspace must not overlap the tensors");
+    const int64_t n_pairs = (M + 255) / 256;
+    if (bh * n_pairs * num_splits > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many work units for one launch");
+    uint32_t* word = nullptr;
+    st = device_setup(true, &word);
+    if (st != FA_OK) return st;
+    CUtensorMap mq, mk, mv;
+    if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
+    if (N > 0) {
+        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+    } else {
+        mk = mq;
+        mv = mq;
+    }
+    fa::Bf16Params p;
+    p.o = o;
+    p.lse = lse;
+    p.err = word;
+    p.bh_count = static_cast<int>(bh);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.n_pairs = static_cast<int>(n_pairs);
+    p.splits = num_splits;
+    p.num_units = static_cast<int>(bh * n_pairs * num_splits);
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = p.ws_o + num_splits * bh * M * D;
+    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (D) {
+        case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
+        case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
+        default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
+    e = fa::launch_combine(p.ws_o, p.ws_lse, o, lse, bh * M, static_cast<int>(D), num_splits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the split merge");
+    return FA_OK;
+}
 
 // ---------------------------------------------------------------------------
 // fa_fwd_noalloc: the bf16 forward for callers that cannot allocate device
@@ -358,7 +458,10 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.n_pairs = static_cast<int>(n_pairs);
+    p.splits = 1;
     p.num_units = static_cast<int>(bh * n_pairs);
+    p.ws_o = nullptr;
+    p.ws_lse = nullptr;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     switch (D) {

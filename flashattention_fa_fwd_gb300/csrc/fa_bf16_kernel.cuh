@@ -13,7 +13,8 @@
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
 // Work unit: one (batch*head, pair of 128-row query tiles). Each CTA is
-// persistent (one per SM) and walks the units u = blockIdx.x, +gridDim.x, ...
+// persistent (one per SM) and takes one unit per round, zigzagging across
+// the grid from round to round (unit_of_round).
 // The two query tiles t = 0, 1 of a unit are processed in ping-pong: while
 // the softmax of one tile runs, the tensor core works on the other tile.
 //
@@ -112,12 +113,23 @@ static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma == 4 * 128, "reg
 
 struct Unit {
     int bh, q0, n0, n1, nmax;
+    int split, kv_lo;   // key-range split of the unit and its first key tile
 };
+
+// Unit a CTA takes in a given round of the persistent loop. Rounds alternate
+// direction ("zigzag"), so that with units ordered heaviest first (causal)
+// the CTA that got a heavy unit in one round gets a light one in the next.
+__device__ __forceinline__ int unit_of_round(int round) {
+    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    return round * G + ((round & 1) ? (G - 1 - b) : b);
+}
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
     Unit U;
     int pair;
+    U.split = u % p.splits;
+    u /= p.splits;
     if (CAUSAL) {
         // Heads in groups of heads_per_group; inside a group the longest
         // query tiles (largest pair index) come first.
@@ -133,9 +145,16 @@ __device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
     }
     U.q0 = pair * 256;
     const int nkv = (p.N + 127) / 128;
-    // Key tiles each query tile visits (0 when the tile lies beyond M).
-    U.n0 = (U.q0 >= p.M) ? 0 : (CAUSAL ? min(nkv, U.q0 / 128 + 1) : nkv);
-    U.n1 = (U.q0 + 128 >= p.M) ? 0 : (CAUSAL ? min(nkv, (U.q0 + 128) / 128 + 1) : nkv);
+    // This split's key tiles are [kv_lo, kv_hi).
+    const int per = (nkv + p.splits - 1) / p.splits;
+    U.kv_lo = min(nkv, U.split * per);
+    const int kv_hi = min(nkv, U.kv_lo + per);
+    // Key tiles each query tile visits (0 when the tile lies beyond M or
+    // the split holds none of its visible keys).
+    const int lim0 = CAUSAL ? min(kv_hi, U.q0 / 128 + 1) : kv_hi;
+    const int lim1 = CAUSAL ? min(kv_hi, (U.q0 + 128) / 128 + 1) : kv_hi;
+    U.n0 = (U.q0 >= p.M) ? 0 : max(0, lim0 - U.kv_lo);
+    U.n1 = (U.q0 + 128 >= p.M) ? 0 : max(0, lim1 - U.kv_lo);
     U.nmax = max(U.n0, U.n1);
     return U;
 }
@@ -171,7 +190,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
     const uint64_t pol_kv = policy_evict_last();
     int kv_idx = 0, qit = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
+        const int u = unit_of_round(round);
+        if (u >= p.num_units) continue;
         const Unit U = unit_info<CAUSAL>(u, p);
         if (U.nmax == 0) continue;
         const int qb = qit % C::QB;
@@ -200,7 +221,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
                 const CUtensorMap* m = which ? mv : mk;
                 for (int pn = 0; pn < C::PANELS; ++pn)
                     tma_load_3d(smem_u32(c.sKV + stage * C::TILE_BYTES + pn * C::PANEL_BYTES), m,
-                                c.bar(C::KV_FULL + stage), pn * 64, j * C::BN, U.bh, pol_kv);
+                                c.bar(C::KV_FULL + stage), pn * 64, (U.kv_lo + j) * C::BN, U.bh, pol_kv);
                 ++kv_idx;
             }
         }
@@ -233,7 +254,9 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
     int pv_cnt[2] = {0, 0};   // P V products issued per query tile
     int units_o[2] = {0, 0};  // units whose last product was committed, per tile
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
+        const int u = unit_of_round(round);
+        if (u >= p.num_units) continue;
         const Unit U = unit_info<CAUSAL>(u, p);
         if (U.nmax == 0) continue;
         const int qb = qit % C::QB;
@@ -322,7 +345,9 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
     const uint64_t c2 = f2_pack(cl2, cl2);
     int s_cnt = 0, st_cnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
+        const int u = unit_of_round(round);
+        if (u >= p.num_units) continue;
         const Unit U = unit_info<CAUSAL>(u, p);
         const int ntile = t ? U.n1 : U.n0;
         if (ntile == 0) continue;
@@ -348,7 +373,7 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
             // The second half is in flight while the first half is reduced.
             tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
             tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-            const int kv0 = j * C::BN;
+            const int kv0 = (U.kv_lo + j) * C::BN;
             const bool need_mask = (kv0 + C::BN > p.N) || (CAUSAL && kv0 + C::BN - 1 > qt0);
             int lim = 128;
             if (need_mask) {
@@ -439,7 +464,9 @@ __device__ __forceinline__ void correction_role(const Bf16Params& p, const Ctx& 
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int a_cnt[2] = {0, 0}, st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
+        const int u = unit_of_round(round);
+        if (u >= p.num_units) continue;
         const Unit U = unit_info<CAUSAL>(u, p);
         for (int j = 0; j < U.nmax && ok; ++j) {
 #pragma unroll
@@ -504,33 +531,58 @@ __device__ __forceinline__ void correction_role(const Bf16Params& p, const Ctx& 
             const int qrow = qt0 + r;
             const bool store = qrow < p.M;
             const float inv_l = (l_fin > 0.f) ? 1.f / l_fin : 0.f;
+            const float lse_val = (l_fin > 0.f) ? (m_fin + log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
             const uint32_t o_addr = c.tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
-            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +   // bf16 bits
-                             (static_cast<size_t>(U.bh) * p.M + (store ? qrow : 0)) * D;
+            const size_t row_idx = static_cast<size_t>(U.bh) * p.M + (store ? qrow : 0);
+            if (p.splits == 1) {
+                uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + row_idx * D;   // bf16 bits
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    if (nt > 0) {
+                        tmem_ld_x32(o_addr + cc * 32, ov);
+                        tmem_ld_wait(ov);
+                    } else {
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t ov[32];
-                if (nt > 0) {
-                    tmem_ld_x32(o_addr + cc * 32, ov);
-                    tmem_ld_wait(ov);
-                } else {
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    uint32_t pkd[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    for (int i = 0; i < 16; ++i)
+                        pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+                    }
                 }
-                uint32_t pkd[16];
+                if (store) p.lse[row_idx] = lse_val;
+            } else {
+                // Split-KV: this split's normalised fp32 O and its LSE go to
+                // the workspace; a second kernel merges the splits.
+                const size_t ws_row = static_cast<size_t>(U.split) * p.bh_count * p.M + row_idx;
+                float* orow = p.ws_o + ws_row * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    if (nt > 0) {
+                        tmem_ld_x32(o_addr + cc * 32, ov);
+                        tmem_ld_wait(ov);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    if (store) {
+                        float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                                 __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
+                    }
                 }
+                if (store) p.ws_lse[ws_row] = lse_val;
             }
-            if (store)
-                p.lse[static_cast<size_t>(U.bh) * p.M + qrow] =
-                    (l_fin > 0.f) ? (m_fin + log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
             if (nt > 0) {
                 tc_fence_before();
                 c.arrive_warp(C::O_FREE + t);

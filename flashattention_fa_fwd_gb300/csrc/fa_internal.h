@@ -20,7 +20,10 @@ struct Bf16Params {
     int M;
     int N;
     int n_pairs;         // ceil(M / 256): units of two 128-row query tiles
-    int num_units;       // bh_count * n_pairs
+    int splits;          // key-range splits per unit (1 = no split)
+    int num_units;       // bh_count * n_pairs * splits
+    float* ws_o;         // splits > 1: [splits, BH, M, D] fp32 partial outputs
+    float* ws_lse;       // splits > 1: [splits, BH, M] fp32 partial log-sum-exps
     int heads_per_group; // causal tile order: heads that share a group
     float scale_log2;    // scale * log2(e)
 };
@@ -50,5 +53,10 @@ struct F32Params {
 };
 
 cudaError_t launch_f32(const F32Params& p, bool causal, cudaStream_t s);
+
+// Merges split-KV partial results: for every row, LSE = ln sum_s exp(LSE_s)
+// and O = sum_s exp(LSE_s - LSE) O_s, written as bf16 O and fp32 LSE.
+cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse, int64_t rows, int D,
+                           int splits, cudaStream_t s);
 
 }  // namespace fa

@@ -108,6 +108,42 @@ fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, f
                      float scale, int causal, void* stream);
 
 /*
+ * Split-KV bf16 forward: the same result as fa_fwd (same arguments, layouts
+ * and checks), computed by cutting each query tile's keys into `num_splits`
+ * contiguous ranges that different CTAs process in parallel, then merging
+ * the partial results with the softmax-of-a-concatenation algebra of
+ * "Module 08: FlashAttention and Memory-Efficient Kernels" (section "Tiling
+ * and the online softmax"): LSE = ln sum_s exp(LSE_s), O = sum_s
+ * exp(LSE_s - LSE) O_s. Useful when B*H*ceil(M/256) is below the SM count
+ * (few query tiles, long keys; "FlashAttention in Triton: A Tile-by-Tile
+ * Walkthrough", section "What the H100 run showed", on exposing more
+ * parallel work).
+ *
+ *   num_splits       1..16; 1 is exactly fa_fwd (the workspace is unused)
+ *   workspace        device memory owned by the caller, 16-byte aligned,
+ *                    at least fa_fwd_splitkv_workspace_bytes(...) bytes, not
+ *                    overlapping the tensors; it holds fp32 partial outputs
+ *                    and log-sum-exps and is overwritten by every call
+ *
+ * Launches two kernels on `stream` (the split kernel, then the merge).
+ * Errors as fa_fwd, plus FA_ERR_INVALID_ARG for num_splits outside [1, 16]
+ * or a missing, short, misaligned or overlapping workspace.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                         float scale, int causal, int num_splits,
+                         void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_splitkv needs: num_splits * B*H*M * (D + 1) * 4
+ * (0 when num_splits == 1; -1 for invalid arguments). Needs no GPU. */
+int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t D, int num_splits);
+
+/* A split count that fills the current device's SMs once with
+ * B*H*ceil(M/256)*splits units, keeping at least two 128-key tiles per
+ * split; 1 for causal problems or when no split helps. */
+int fa_fwd_splitkv_suggest(int64_t B, int64_t H, int64_t M, int64_t N, int causal);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns FA_ERR_TIMEOUT if a kernel launched since the last call gave
  * up on a pipeline wait (its outputs are then undefined), FA_ERR_CUDA if the

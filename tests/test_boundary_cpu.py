@@ -106,3 +106,20 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(_binding, "_LIB_PATH", "/nonexistent/libfa_fwd.so")
     with pytest.raises(RuntimeError, match="not built"):
         _binding.load_library()
+
+
+def test_splitkv_workspace_size_and_checks(lib):
+    # num_splits * B*H*M * (D + 1) * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 1000, 96, 3) == 3 * 16 * 1000 * 97 * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 1000, 96, 1) == 0
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 8, 1000, 96, 0) == -1
+    need = fa.fa_fwd_splitkv_workspace_bytes(1, 2, 256, 64, 2)
+    W = 64 * A
+    args = (*PTRS, 1, 2, 256, 512, 64, 0.125, False)
+    assert fa.fa_fwd_splitkv_raw(*args, 2, W, need - 4, 0) == fa.FA_ERR_INVALID_ARG     # too small
+    assert fa.fa_fwd_splitkv_raw(*args, 2, 0, need, 0) == fa.FA_ERR_INVALID_ARG          # missing
+    assert fa.fa_fwd_splitkv_raw(*args, 2, W + 4, need, 0) == fa.FA_ERR_INVALID_ARG      # misaligned
+    assert fa.fa_fwd_splitkv_raw(*args, 2, A, need, 0) == fa.FA_ERR_INVALID_ARG          # overlaps q
+    assert fa.fa_fwd_splitkv_raw(*args, 17, W, need, 0) == fa.FA_ERR_INVALID_ARG         # too many splits
+    assert fa.fa_fwd_splitkv_raw(A, 2 * A, 3 * A, 4 * A, 5 * A, 0, 2, 256, 512, 64, 0.125, False,
+                                 2, W, need, 0) == fa.FA_OK                                # empty problem

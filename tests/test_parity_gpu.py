@@ -211,3 +211,44 @@ def test_full_long_causal_64k_sampled_rows():
     """256 seeded rows per head, all 8 heads, against the 64K-key oracle."""
     w = WORKLOADS["long_causal_b1_h8_s65536_d64"]
     _full_size_check(w, heads=list(range(w.B * w.H)), rows_per_head=256)
+
+
+# ------------------------------------------------------------------ split-KV
+
+def run_splitkv(q, k, v, scale, causal, splits):
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from parity import to_device_bf16
+
+    tq, tk, tv = (to_device_bf16(x) for x in (q, k, v))
+    o = torch.full_like(tq, float("nan"))
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_splitkv(tq, tk, tv, o, lse, scale, causal, num_splits=splits)
+    assert fa.fa_get_device_status() == fa.FA_OK
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("splits", [2, 3, 0])
+def test_splitkv_ragged_cross_workload(splits):
+    """The low-parallelism workload (16 heads x 4 query-tile pairs) with its
+    3000 keys cut into ranges; 0 = the library's suggested split count."""
+    w = WORKLOADS["cross_b2_h8_m1000_n3000_d96_peaked"]
+    q, k, v = make_inputs(w)
+    o, lse = run_splitkv(q, k, v, w.scale, w.causal, splits)
+    o_ref, lse_ref = attention(q, k, v, w.scale, w.causal)
+    check_bf16(o, lse, o_ref, lse_ref, f"{w.name} splits={splits}")
+
+
+@pytest.mark.parametrize("D", [64, 96, 128])
+@pytest.mark.parametrize("causal,M,N,splits", [(False, 300, 700, 2), (False, 300, 700, 4), (True, 600, 600, 3),
+                                               (False, 130, 200, 4), (True, 1, 300, 2), (True, 300, 200, 5)])
+def test_splitkv_shapes(D, causal, M, N, splits):
+    """Ragged tails, causal rows whose visible keys lie in fewer splits than
+    there are, and more splits than key tiles (empty splits)."""
+    q = _rand((1, 3, M, D), 51 + M + N + splits)
+    k = _rand((1, 3, N, D), 52 + M + N + splits)
+    v = _rand((1, 3, N, D), 53 + M + N + splits)
+    o, lse = run_splitkv(q, k, v, 1 / math.sqrt(D), causal, splits)
+    o_ref, lse_ref = attention(q, k, v, 1 / math.sqrt(D), causal)
+    check_bf16(o, lse, o_ref, lse_ref, f"splitkv M{M} N{N} D{D} causal={causal} splits={splits}")
