@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU seconds for the oracle sample")
+    ap.add_argument("--splitkv", type=int, default=None, metavar="S",
+                    help="time fa_fwd_splitkv with S key-range splits (0 = the library's suggestion)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
     return ap.parse_args(argv)
@@ -288,6 +290,14 @@ def gpu_arm(args, w, rank, world, local_rank):
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.M, dtype=torch.float32, device=dev)
     call = fa.fa_fwd if bf16 else fa.fa_fwd_f32
+    splits = 1
+    if args.splitkv is not None and bf16:
+        splits = args.splitkv or fa.fa_fwd_splitkv_suggest(w.B, w.H, w.M, w.N, w.causal)
+        ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.M, w.D, splits), 16),
+                         dtype=torch.uint8, device=dev)
+
+        def call(q_, k_, v_, o_, l_, scale_, causal_):
+            fa.fa_fwd_splitkv(q_, k_, v_, o_, l_, scale_, causal_, num_splits=splits, workspace=ws)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -386,7 +396,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": max_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
-        "config": dict(w.describe(), parallelism=f"replicas x{world}",
+        "config": dict(w.describe(), parallelism=f"replicas x{world}", kv_splits=splits,
                        l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
                        if in_bytes > 129e6 else "inputs fit in L2 (warm)"),
         "pct_of_peak": 100.0 * value / world / peak,
@@ -399,7 +409,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps},
-        "gpu_launches": steps,
+        "gpu_launches": steps * (2 if splits > 1 else 1),
         "clocks": clocks,
         "clocks_rejected": clocks_rejected(clocks),
     }

@@ -1,14 +1,14 @@
 // bf16 FlashAttention forward for sm_103a: TMA-fed shared-memory tiles,
 // tcgen05 MMAs with fp32 accumulators in tensor memory, warp-specialised
-// load / MMA / softmax / correction roles, persistent CTAs.
+// load / MMA / softmax / epilogue roles, persistent CTAs.
 //
 // Algorithm ("FlashAttention-style kernel", section "The loop"; "Module 08:
 // FlashAttention and Memory-Efficient Kernels", sections "Tiling and the
 // online softmax" and "Related ideas"): a query tile stays resident while
 // key/value tiles stream past it; per row the kernel carries the running
 // max m, the running sum l and the unnormalised output acc, rescales l and
-// acc by alpha = exp2(m_old - m_new) whenever the max grows, and divides by
-// l once at the end. log2(e) is folded into the score scale so that each
+// acc by alpha = exp2(m_old - m_new) when the max grows (see "Running max"
+// below), and divides by l once at the end. log2(e) is folded into the score scale so that each
 // score costs one FMA and one base-two exponential. The per-row log-sum-exp
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
@@ -21,8 +21,8 @@
 // Roles (512 threads, 4 warpgroups; registers re-split with setmaxnreg):
 //   WG0 (warps 0-3)   softmax of query tile 0   (thread = row = TMEM lane)
 //   WG1 (warps 4-7)   softmax of query tile 1
-//   WG2 (warps 8-11)  correction (rescales O by alpha while the softmax
-//                     computes the exponentials) and epilogue (O / l, LSE)
+//   WG2 (warps 8-11)  epilogue (O / l, LSE) of the previous unit while the
+//                     next one runs
 //   WG3 (warps 12-15) warp 12: TMA producer; warp 13: tensor-memory owner
 //                     and MMA issuer; warps 14-15 idle
 //
@@ -38,18 +38,20 @@
 // tcgen05 MMAs from one thread execute in issue order, so S_t(j) only
 // overwrites P_t(j-1) after the product that reads it, and the commit that
 // announces S_t(j) also guarantees that O_t holds every earlier product
-// (which is what lets the correction warps rescale O_t before P_t(j) V(j)).
+// (which is what lets the softmax rescale O_t before P_t(j) V(j)).
 //
-// Hand-offs per tile j of query tile t (mbarriers):
-//   S_FULL  MMA -> softmax        S_t(j) is in tensor memory
-//   A_FULL  softmax -> correction alpha(j) is in shared memory (sent right
-//                                 after the row max, before the exponentials)
-//   P_FULL  softmax -> MMA        P_t(j) is in tensor memory
-//   O_READY correction -> MMA     O_t has been rescaled by alpha(j)
-// per unit: ST_FULL (softmax -> epilogue: final m, l), O_DONE (MMA ->
-// epilogue: last product done), O_FREE (epilogue -> MMA: O_t may be
-// overwritten by the next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY
-// (TMA ring).
+// Running max: a row's reference m (shared by l and acc) moves only when a
+// tile raises the row max by more than 2^8; then alpha = exp2(m_old - m_new)
+// rescales l and acc, as in the pages' recurrence. Below that the stale
+// reference is exact for O = acc / l and LSE = m + log l; the one bf16
+// effect it has -- the tile's largest weight can exceed 1 and is rounded
+// when it enters P V -- is compensated by normalising O with l_o, which
+// counts each tile's largest weight as rounded.
+//
+// Hand-offs (mbarriers): S_FULL (MMA -> softmax), P_FULL (softmax -> MMA),
+// per unit ST_FULL / ST_EMPTY (softmax <-> epilogue: m, l, l_o), O_DONE
+// (MMA -> epilogue), O_FREE (epilogue -> MMA: O_t may be overwritten by the
+// next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY (TMA ring).
 //
 // Causal (top-left, key j visible to query i when j <= i): key tiles wholly
 // above the diagonal are never loaded or multiplied; the diagonal tile and a
@@ -93,14 +95,13 @@ struct Bf16Cfg {
     // shared memory layout (offsets from a 1024-byte aligned base)
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = Q_OFF + QB * 2 * TILE_BYTES;
-    static constexpr int ALPHA_OFF = KV_OFF + NS * TILE_BYTES;      // float [2][128]
-    static constexpr int STATS_OFF = ALPHA_OFF + 2 * 128 * 4;       // float [2 buf][2 t][2][128]
-    static constexpr int BAR_OFF = STATS_OFF + 2 * 2 * 2 * 128 * 4;
+    static constexpr int STATS_OFF = KV_OFF + NS * TILE_BYTES;      // float [2 t][3 (m, l, l_o)][128]
+    static constexpr int BAR_OFF = STATS_OFF + 2 * 3 * 128 * 4;
     // barrier slots
     static constexpr int KV_FULL = 0, KV_EMPTY = NS, Q_FULL = 2 * NS, Q_EMPTY = 2 * NS + QB;
-    static constexpr int S_FULL = 2 * NS + 2 * QB, P_FULL = S_FULL + 2, A_FULL = S_FULL + 4;
-    static constexpr int O_READY = S_FULL + 6, O_DONE = S_FULL + 8, O_FREE = S_FULL + 10;
-    static constexpr int ST_FULL = S_FULL + 12, DRAIN = S_FULL + 14;
+    static constexpr int S_FULL = 2 * NS + 2 * QB, P_FULL = S_FULL + 2, O_DONE = S_FULL + 4;
+    static constexpr int O_FREE = S_FULL + 6, ST_FULL = S_FULL + 8, ST_EMPTY = S_FULL + 10;
+    static constexpr int DRAIN = S_FULL + 12;
     static constexpr int NUM_BARS = DRAIN + 1;
     static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -108,8 +109,12 @@ struct Bf16Cfg {
 
 // Register split per warpgroup (setmaxnreg); sums to 512 x 128, the launch's
 // registers, and to 512 per SM sub-partition (one warp of each group).
-constexpr int kRegsSoftmax = 176, kRegsCorrection = 64, kRegsLoadMma = 96;
-static_assert(2 * kRegsSoftmax + kRegsCorrection + kRegsLoadMma == 4 * 128, "register split");
+constexpr int kRegsSoftmax = 176, kRegsEpilogue = 64, kRegsLoadMma = 96;
+static_assert(2 * kRegsSoftmax + kRegsEpilogue + kRegsLoadMma == 4 * 128, "register split");
+
+// A row's running max (the reference of its l and acc) only moves when a
+// tile raises the max by more than this, in base-2 units (a factor 256).
+constexpr float kRescaleLog2 = 8.0f;
 
 struct Unit {
     int bh, q0, n0, n1, nmax;
@@ -163,8 +168,7 @@ struct Ctx {
     uint32_t bar0;        // shared address of barrier 0
     uint8_t* sQ;
     uint8_t* sKV;
-    float* alpha_sm;      // [2][128]
-    float* stats_sm;      // [2 buf][2 t][2 (m, l)][128]
+    float* stats_sm;      // [2 t][3 (m, l, l_o)][128]
     uint32_t tmem;
     volatile int* abort;
     uint32_t* err;
@@ -277,7 +281,7 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
                 const uint32_t s_col = t ? C::S_COL1 : C::S_COL0;
                 const uint32_t o_col = t ? C::O_COL1 : C::O_COL0;
                 if (ok && j >= 1 && j - 1 < nt) {
-                    ok = c.wait(C::P_FULL + t, pv_cnt[t]) && c.wait(C::O_READY + t, pv_cnt[t]);
+                    ok = c.wait(C::P_FULL + t, pv_cnt[t]);
                     // The first product of a unit overwrites O_t: the
                     // previous unit's epilogue must have read it.
                     if (ok && j == 1 && units_o[t] > 0) ok = c.wait(C::O_FREE + t, units_o[t] - 1);
@@ -340,7 +344,8 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = (warp & 3) * 32 + lane;                   // row in the tile = TMEM lane
-    const uint32_t s_addr = c.tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t lane_base = c.tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_addr = lane_base + (t ? C::S_COL1 : C::S_COL0);
     const float cl2 = p.scale_log2;
     const uint64_t c2 = f2_pack(cl2, cl2);
     int s_cnt = 0, st_cnt = 0;
@@ -355,6 +360,7 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
         const int qrow = qt0 + r;
         float m_run = -INFINITY;   // running max of scaled scores, base-2 units
         float l_run = 0.f;         // running sum of exp2(score - m_run)
+        float lo_run = 0.f;        // l with each tile's largest weight as rounded to bf16
         for (int j = 0; j < ntile; ++j) {
             // Every lane must agree: the tensor-memory loads below are
             // warp-collective.
@@ -409,16 +415,16 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
                 mx3 = fmax3(mx3, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
             }
             const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            // New running max; alpha rescales what was accumulated so far
-            // (1 for rows whose max did not move). It goes to the correction
-            // warps now, so that the rescale of O overlaps the exponentials.
-            const float m_tile = mx * cl2;                   // -inf if all masked
-            const bool grow = m_tile > m_run;                // first visible tile: m_run = -inf
+            // Running max m_run: the common reference of l and acc. It moves
+            // only when a tile raises the row max by more than kRescaleLog2
+            // (then alpha rescales what was accumulated, as on the pages);
+            // below that p = exp2(s*c - m_run) <= 2^kRescaleLog2 and nothing
+            // needs rescaling, which makes the rescale of O rare.
+            const float m_tile = mx * cl2;                         // -inf if all masked
+            const bool grow = m_tile > m_run + kRescaleLog2;       // first visible tile: m_run = -inf
             const float m_new = grow ? m_tile : m_run;
             const float alpha = grow ? ex2(m_run - m_new) : 1.f;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // no -inf - -inf
-            c.alpha_sm[t * 128 + r] = alpha;
-            c.arrive_warp(C::A_FULL + t);
             const uint64_t neg2 = f2_pack(-m_use, -m_use);
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[64];
@@ -432,88 +438,83 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
                 acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(p0, p1));
                 pk[i] = pack_bf16x2(p0, p1);
             }
+            // The tile's largest weight exactly as the MMA will see it (same
+            // FMA and exp2 as in the loop, then bf16): its rounding error
+            // goes into l_o, the normaliser of O, so a dominant key is not
+            // misweighted when the reference is stale (p_max may be > 1).
+            const float pmax = ex2(fmaf(mx, cl2, -m_use));
+            const float pmax_b = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
             tmem_st_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
             tmem_st_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            // A moved reference: rescale this warp's rows of O. S_t(j) was
+            // issued after P_t(j-1) V(j-1), so that product has landed; tile 0
+            // of a unit has no accumulator yet (its first product overwrites).
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                const uint32_t o_addr = lane_base + (t ? C::O_COL1 : C::O_COL0);
+                const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld_x32(o_addr + cc * 32, ov);
+                    tmem_ld_wait(ov);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float lo, hi;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])), a2, 0ull), lo, hi);
+                        ov[2 * i] = __float_as_uint(lo);
+                        ov[2 * i + 1] = __float_as_uint(hi);
+                    }
+                    tmem_st_x32(o_addr + cc * 32, ov);
+                }
+            }
             float sa, sb, sc, sd;
             f2_unpack(f2_add(acc2[0], acc2[1]), sa, sb);
             f2_unpack(f2_add(acc2[2], acc2[3]), sc, sd);
-            l_run = l_run * alpha + ((sa + sb) + (sc + sd));
+            const float lsum = (sa + sb) + (sc + sd);
+            l_run = l_run * alpha + lsum;
+            lo_run = lo_run * alpha + (lsum + (pmax_b - pmax));
             m_run = m_new;
             tmem_st_wait();
             tc_fence_before();
             c.arrive_warp(C::P_FULL + t);
         }
         if (!ok) break;
-        // Final statistics of this tile for the epilogue (double-buffered by
-        // unit, so the next unit's values never overwrite unread ones).
-        float* st = c.stats_sm + ((st_cnt & 1) * 2 + t) * 256;
+        // Final statistics of this tile for the epilogue, once it has read
+        // the previous unit's (ST_EMPTY): that also keeps ST_FULL at most one
+        // phase ahead of its waiter.
+        if (st_cnt > 0 && !c.wait_warp(C::ST_EMPTY + t, st_cnt - 1)) break;
+        float* st = c.stats_sm + t * 384;
         st[r] = m_run;
         st[128 + r] = l_run;
+        st[256 + r] = lo_run;
         c.arrive_warp(C::ST_FULL + t);
         ++st_cnt;
     }
 }
 
-// ------------------------------------------------ correction and epilogue
+// --------------------------------------------------------------- epilogue
+// Per unit and query tile: O = acc / l_o in bf16 (or the split's fp32 partial
+// result), LSE = ln2 * (m + log2 l).
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void correction_role(const Bf16Params& p, const Ctx& c) {
+__device__ __forceinline__ void epilogue_role(const Bf16Params& p, const Ctx& c) {
     using C = Bf16Cfg<D>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int a_cnt[2] = {0, 0}, st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
+    int st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
     bool ok = true;
     for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
         const int u = unit_of_round(round);
         if (u >= p.num_units) continue;
         const Unit U = unit_info<CAUSAL>(u, p);
-        for (int j = 0; j < U.nmax && ok; ++j) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (!ok || j >= (t ? U.n1 : U.n0)) continue;
-                if (!c.wait_warp(C::A_FULL + t, a_cnt[t])) {
-                    ok = false;
-                    break;
-                }
-                ++a_cnt[t];
-                if (j > 0) {
-                    const float alpha = c.alpha_sm[t * 128 + r];
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                        tc_fence_after();
-                        const uint32_t o_addr = c.tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
-                        const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t ov[32];
-                            tmem_ld_x32(o_addr + cc * 32, ov);
-                            tmem_ld_wait(ov);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const uint64_t v2 = f2_fma(f2_pack(__uint_as_float(ov[2 * i]), __uint_as_float(ov[2 * i + 1])),
-                                                           a2, 0ull);
-                                float lo, hi;
-                                f2_unpack(v2, lo, hi);
-                                ov[2 * i] = __float_as_uint(lo);
-                                ov[2 * i + 1] = __float_as_uint(hi);
-                            }
-                            tmem_st_x32(o_addr + cc * 32, ov);
-                        }
-                        tmem_st_wait();
-                    }
-                }
-                tc_fence_before();
-                c.arrive_warp(C::O_READY + t);
-            }
-        }
-        if (!ok) break;
         // Epilogue: O = acc / l in bf16, LSE = ln2 * (m + log2 l).
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const int nt = t ? U.n1 : U.n0;
             const int qt0 = U.q0 + 128 * t;
             if (!ok || qt0 >= p.M) continue;
-            float m_fin = -INFINITY, l_fin = 0.f;
+            float m_fin = -INFINITY, l_fin = 0.f, lo_fin = 0.f;
             if (nt > 0) {
                 bool w = c.wait_warp(C::ST_FULL + t, st_cnt[t]);
                 w = w && c.wait_warp(C::O_DONE + t, od_cnt[t]);
@@ -521,16 +522,18 @@ __device__ __forceinline__ void correction_role(const Bf16Params& p, const Ctx& 
                     ok = false;
                     break;
                 }
-                const float* st = c.stats_sm + ((st_cnt[t] & 1) * 2 + t) * 256;
+                const float* st = c.stats_sm + t * 384;
                 m_fin = st[r];
                 l_fin = st[128 + r];
+                lo_fin = st[256 + r];
+                c.arrive_warp(C::ST_EMPTY + t);
                 ++st_cnt[t];
                 ++od_cnt[t];
                 tc_fence_after();
             }
             const int qrow = qt0 + r;
             const bool store = qrow < p.M;
-            const float inv_l = (l_fin > 0.f) ? 1.f / l_fin : 0.f;
+            const float inv_l = (lo_fin > 0.f) ? 1.f / lo_fin : 0.f;
             const float lse_val = (l_fin > 0.f) ? (m_fin + log2f(l_fin)) * 0.69314718055994531f : -INFINITY;
             const uint32_t o_addr = c.tmem + lane_base + (t ? C::O_COL1 : C::O_COL0);
             const size_t row_idx = static_cast<size_t>(U.bh) * p.M + (store ? qrow : 0);
@@ -607,7 +610,6 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     c.bar0 = smem_u32(smem + C::BAR_OFF);
     c.sQ = smem + C::Q_OFF;
     c.sKV = smem + C::KV_OFF;
-    c.alpha_sm = reinterpret_cast<float*>(smem + C::ALPHA_OFF);
     c.stats_sm = reinterpret_cast<float*>(smem + C::STATS_OFF);
     c.abort = &abort_sh;
     c.err = p.err;
@@ -625,11 +627,10 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         for (int t = 0; t < 2; ++t) {
             mbar_init(c.bar(C::S_FULL + t), 1);
             mbar_init(c.bar(C::P_FULL + t), 128);
-            mbar_init(c.bar(C::A_FULL + t), 128);
-            mbar_init(c.bar(C::O_READY + t), 128);
             mbar_init(c.bar(C::O_DONE + t), 1);
             mbar_init(c.bar(C::O_FREE + t), 128);
             mbar_init(c.bar(C::ST_FULL + t), 128);
+            mbar_init(c.bar(C::ST_EMPTY + t), 128);
         }
         mbar_init(c.bar(C::DRAIN), 1);
         fence_barrier_init();
@@ -653,8 +654,8 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
         setmaxnreg_inc<kRegsSoftmax>();
         softmax_role<D, CAUSAL>(wg, p, c);
     } else if (wg == 2) {
-        setmaxnreg_dec<kRegsCorrection>();
-        correction_role<D, CAUSAL>(p, c);
+        setmaxnreg_dec<kRegsEpilogue>();
+        epilogue_role<D, CAUSAL>(p, c);
     } else {
         setmaxnreg_dec<kRegsLoadMma>();
         if (warp == 12) {
