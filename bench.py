@@ -182,36 +182,39 @@ def whole_job_value(flops_per_step: float, steps: int, world: int, max_ms: float
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, target_s: float):
-    """Times the fp64 oracle on sampled query rows of head 0 of workload w.
+    """Times the fp64 oracle on sampled query rows of workload w's heads.
 
     Returns (TFLOP/s under the metric's convention, seconds, rows, cores,
-    description). The sample grows until it takes about target_s seconds.
+    description). Heads are added (256 sampled rows each, all rows when M is
+    smaller) until the sample has taken about target_s seconds.
     """
     import numpy as np
 
     from flashattention_fa_fwd_gb300.inputs import head_tensor, sample_rows
     from oracle import attention_rows
 
-    qh = head_tensor(w.wid, 0, 0, w.M, w.D, w.sigma_qk, w.dtype)
-    kh = head_tensor(w.wid, 1, 0, w.N, w.D, w.sigma_qk, w.dtype)
-    vh = head_tensor(w.wid, 2, 0, w.N, w.D, w.sigma_v, w.dtype)
-
-    def flops_of(rows):
-        vis = np.minimum(rows + 1, w.N) if w.causal else np.full(rows.size, w.N)
-        return 4.0 * w.D * float(vis.sum())
-
-    count = min(w.M, 32)
-    while True:
-        rows = sample_rows(w.wid, 0, w.M, count)
+    flops = 0.0
+    secs = 0.0
+    nrows = 0
+    heads = 0
+    for bh in range(w.B * w.H):
+        qh = head_tensor(w.wid, 0, bh, w.M, w.D, w.sigma_qk, w.dtype)
+        kh = head_tensor(w.wid, 1, bh, w.N, w.D, w.sigma_qk, w.dtype)
+        vh = head_tensor(w.wid, 2, bh, w.N, w.D, w.sigma_v, w.dtype)
+        rows = sample_rows(w.wid, bh, w.M, 256)
         t0 = time.perf_counter()
         attention_rows(qh, kh, vh, w.scale, w.causal, rows)
-        dt = time.perf_counter() - t0
-        if dt >= 0.25 * target_s or count >= w.M:
+        secs += time.perf_counter() - t0
+        vis = np.minimum(rows + 1, w.N) if w.causal else np.full(rows.size, w.N)
+        flops += 4.0 * w.D * float(vis.sum())
+        nrows += int(rows.size)
+        heads += 1
+        if secs >= target_s:
             break
-        count = min(w.M, max(count * 2, int(count * 0.3 * target_s / max(dt, 1e-3))))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    desc = f"{rows.size} sampled query rows of head 0 of {w.name} ({w.N} keys each, fp64 numpy)"
-    return flops_of(rows) / dt / 1e12, dt, int(rows.size), int(cores), desc
+    desc = (f"{nrows} sampled query rows over {heads} heads of {w.name} ({w.N} keys each, fp64 numpy oracle, "
+            f"{secs:.1f} s)")
+    return flops / secs / 1e12, secs, nrows, int(cores), desc
 
 
 def oracle_step_fn(w, rows_per_step: int):
