@@ -103,7 +103,10 @@ struct Bf16Cfg {
     static constexpr int O_FREE = S_FULL + 6, ST_FULL = S_FULL + 8, ST_EMPTY = S_FULL + 10;
     static constexpr int DRAIN = S_FULL + 12;
     static constexpr int NUM_BARS = DRAIN + 1;
-    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + NUM_BARS * 8;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;         // tensor-memory base, abort flag
+    static constexpr int SMEM_USED = MISC_OFF + 16;
+    // + slack to align the base up to 1024 B (the 128-byte swizzle atom).
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -213,6 +216,19 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
                             c.bar(C::Q_FULL + qb), pn * 64, U.q0 + 128 * t, U.bh, pol_q);
         }
         ++qit;
+        if (C::QB == 1) {
+            // One Q buffer: the next unit's Q tiles can only be loaded once
+            // this unit's last Q K^T product is done. Pull them into L2 now so
+            // that load does not wait on HBM.
+            const int un = unit_of_round(round + 1);
+            if (un < p.num_units) {
+                const Unit N = unit_info<CAUSAL>(un, p);
+                for (int t = 0; t < 2; ++t) {
+                    if ((t ? N.n1 : N.n0) == 0) continue;
+                    for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(mq, pn * 64, N.q0 + 128 * t, N.bh);
+                }
+            }
+        }
         for (int j = 0; j < U.nmax && ok; ++j) {
             for (int which = 0; which < 2; ++which) {
                 const int stage = kv_idx % C::NS;
@@ -599,10 +615,12 @@ __global__ void __launch_bounds__(Bf16Cfg<D>::THREADS, 1)
 fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const Bf16Params p) {
     using C = Bf16Cfg<D>;
+    // All shared state lives in the dynamic window (no static shared
+    // variables), aligned up to 1024 B inside the launch's slack.
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int abort_sh;
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+    int& abort_sh = *reinterpret_cast<int*>(smem + C::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
