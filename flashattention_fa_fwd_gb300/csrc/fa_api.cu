@@ -3,8 +3,10 @@
 // Validates arguments before anything touches the GPU, builds the TMA
 // tensor maps, picks the kernel for the head dimension and launches it on
 // the caller's stream. The library never synchronises inside fa_fwd /
-// fa_fwd_f32 and allocates nothing per call; the only allocation is one
-// 4-byte status word per device, made on the first call on that device.
+// fa_fwd_f32 and allocates nothing per call; the only allocation is one small
+// block of device state per device (the status word and the work counters
+// of the bf16 kernel's unit scheduler), made on the first call on that
+// device.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -12,6 +14,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -37,15 +40,27 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
+// Work-counter slots of the bf16 kernel's unit scheduler: each launch takes
+// the next slot in turn, so up to this many launches may run at once (on
+// different streams) without sharing a counter.
+constexpr int kSchedSlots = 64;
+struct DeviceState {
+    uint32_t status;                 // the device status word
+    uint32_t pad;
+    int sched[kSchedSlots][2];       // per launch: next unit, CTAs finished
+};
 std::mutex g_mu;
 uint32_t* g_status_word[kMaxDevices] = {};
+DeviceState* g_state[kMaxDevices] = {};
+std::atomic<uint32_t> g_launch_seq[kMaxDevices];
 int g_arch[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// Per-device set-up on first use: architecture check, status word, and the
-// driver's tensor-map encoder (fetched through the runtime, so the library
-// does not link libcuda).
-fa_status device_setup(bool need_encoder, uint32_t** status_word) {
+// Per-device set-up on first use: architecture check, device state (status
+// word, work counters), and the driver's tensor-map encoder (fetched through
+// the runtime, so the library does not link libcuda). *sched, when asked
+// for, receives the work-counter slot of this launch.
+fa_status device_setup(bool need_encoder, uint32_t** status_word, int** sched = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -59,17 +74,18 @@ fa_status device_setup(bool need_encoder, uint32_t** status_word) {
         g_arch[dev] = (major == 10 && minor == 3) ? 1 : -1;
     }
     if (g_arch[dev] != 1) return fail(FA_ERR_UNSUPPORTED, "device %d is not sm_103 (this library is built for sm_103a only)", dev);
-    if (g_status_word[dev] == nullptr) {
-        uint32_t* w = nullptr;
-        e = cudaMalloc(&w, sizeof(uint32_t));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status word)");
-        e = cudaMemset(w, 0, sizeof(uint32_t));
+    if (g_state[dev] == nullptr) {
+        DeviceState* w = nullptr;
+        e = cudaMalloc(&w, sizeof(DeviceState));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(device state)");
+        e = cudaMemset(w, 0, sizeof(DeviceState));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
             cudaFree(w);
-            return cuda_fail(e, "clearing the status word");
+            return cuda_fail(e, "clearing the device state");
         }
-        g_status_word[dev] = w;
+        g_state[dev] = w;
+        g_status_word[dev] = &w->status;
     }
     if (need_encoder && g_encode == nullptr) {
         void* fn = nullptr;
@@ -80,6 +96,10 @@ fa_status device_setup(bool need_encoder, uint32_t** status_word) {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     *status_word = g_status_word[dev];
+    if (sched != nullptr) {
+        const uint32_t slot = g_launch_seq[dev].fetch_add(1, std::memory_order_relaxed) % kSchedSlots;
+        *sched = g_state[dev]->sched[slot];
+    }
     return FA_OK;
 }
 
@@ -152,7 +172,8 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     const int64_t n_pairs = (M + 255) / 256;
     if (bh * n_pairs > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many query tiles for one launch");
     uint32_t* word = nullptr;
-    st = device_setup(true, &word);
+    int* sched = nullptr;
+    st = device_setup(true, &word, &sched);
     if (st != FA_OK) return st;
 
     CUtensorMap mq, mk, mv;
@@ -178,6 +199,7 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.ws_lse = nullptr;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    p.sched = sched;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
@@ -313,7 +335,8 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     const int64_t n_pairs = (M + 255) / 256;
     if (bh * n_pairs * num_splits > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many work units for one launch");
     uint32_t* word = nullptr;
-    st = device_setup(true, &word);
+    int* sched = nullptr;
+    st = device_setup(true, &word, &sched);
     if (st != FA_OK) return st;
     CUtensorMap mq, mk, mv;
     if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
@@ -338,6 +361,7 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     p.ws_lse = p.ws_o + num_splits * bh * M * D;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    p.sched = sched;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
@@ -355,8 +379,9 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
 // fa_fwd_noalloc: the bf16 forward for callers that cannot allocate device
 // memory.
 //
-// fa_fwd keeps its device status word (the kernel's only scratch memory) in
-// a buffer it cudaMallocs on its first call on each device. Some callers
+// fa_fwd keeps the kernel's scratch memory (its status word and the work
+// counters its CTAs claim units from) in a buffer it cudaMallocs on its
+// first call on each device. Some callers
 // cannot allow that: applications whose own caching allocator or memory
 // pool already owns all device memory (a cudaMalloc from a library can fail
 // or defragment their pool), serving loops that must not take the implicit
@@ -381,9 +406,10 @@ constexpr int kNoAllocScratchWords = 64;
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
 uint32_t* g_noalloc_scratch_addr[kMaxDevices] = {};
 
-// Words of scratch the bf16 kernel needs: its status word, whatever the
-// problem size.
-constexpr int kBf16ScratchWords = 1;
+// Words of scratch the bf16 kernel needs, whatever the problem size: its
+// status word (word 0) and the two counters of its unit scheduler (words 1
+// and 2: next unit to claim, CTAs finished).
+constexpr int kBf16ScratchWords = 3;
 
 fa_status noalloc_setup(uint32_t** scratch) {
     int dev = 0;
@@ -464,6 +490,7 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
     p.ws_lse = nullptr;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+    p.sched = reinterpret_cast<int*>(scratch + 1);
     switch (D) {
         case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
         case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;

@@ -13,8 +13,11 @@
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
 // Work unit: one (batch*head, pair of 128-row query tiles). Each CTA is
-// persistent (one per SM) and takes one unit per round, zigzagging across
-// the grid from round to round (unit_of_round).
+// persistent (one per SM) and claims units one at a time from a global
+// counter, in an order that puts the longest causal units of a group of
+// heads first (unit_info), so that CTAs finish within one short unit of each
+// other. The CTA's TMA thread claims each unit and passes its index to the
+// other roles through a small ring in shared memory (UNIT_FULL / UNIT_EMPTY).
 // The two query tiles t = 0, 1 of a unit are processed in ping-pong: while
 // the softmax of one tile runs, the tensor core works on the other tile.
 //
@@ -102,9 +105,15 @@ struct Bf16Cfg {
     static constexpr int S_FULL = 2 * NS + 2 * QB, P_FULL = S_FULL + 2, O_DONE = S_FULL + 4;
     static constexpr int O_FREE = S_FULL + 6, ST_FULL = S_FULL + 8, ST_EMPTY = S_FULL + 10;
     static constexpr int DRAIN = S_FULL + 12;
-    static constexpr int NUM_BARS = DRAIN + 1;
+    static constexpr int UNIT_SLOTS = 4;                            // ring of claimed unit indices
+    static constexpr int UNIT_FULL = DRAIN + 1, UNIT_EMPTY = UNIT_FULL + UNIT_SLOTS;
+    // Readers of a ring slot: the MMA thread, and one lane of each of the
+    // four warps of both softmax warpgroups and of the epilogue warpgroup.
+    static constexpr int UNIT_READERS = 1 + 3 * 4;
+    static constexpr int NUM_BARS = UNIT_EMPTY + UNIT_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;         // tensor-memory base, abort flag
-    static constexpr int SMEM_USED = MISC_OFF + 16;
+    static constexpr int RING_OFF = MISC_OFF + 16;                  // int [UNIT_SLOTS]
+    static constexpr int SMEM_USED = RING_OFF + UNIT_SLOTS * 4;
     // + slack to align the base up to 1024 B (the 128-byte swizzle atom).
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -123,14 +132,6 @@ struct Unit {
     int bh, q0, n0, n1, nmax;
     int split, kv_lo;   // key-range split of the unit and its first key tile
 };
-
-// Unit a CTA takes in a given round of the persistent loop. Rounds alternate
-// direction ("zigzag"), so that with units ordered heaviest first (causal)
-// the CTA that got a heavy unit in one round gets a light one in the next.
-__device__ __forceinline__ int unit_of_round(int round) {
-    const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-    return round * G + ((round & 1) ? (G - 1 - b) : b);
-}
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
@@ -186,6 +187,32 @@ struct Ctx {
     // Per-thread arrive (the hand-off barriers count the 128 threads of a
     // warpgroup).
     __device__ __forceinline__ void arrive_warp(int i) const { mbar_arrive(bar(i)); }
+    volatile int* ring;   // claimed unit indices, -1 = no more units
+};
+
+// The sequence of units this CTA processes, as every role but the TMA thread
+// reads it from the ring: next() returns the following unit index, or -1
+// when there are no more units (or the pipeline was aborted). `whole_warp`
+// readers call it with all 32 lanes and arrive once per warp; the MMA thread
+// calls it alone.
+template <int SLOTS, int FULL, int EMPTY>
+struct UnitReader {
+    int k = 0;
+    __device__ __forceinline__ int next(const Ctx& c, bool whole_warp) {
+        const int slot = k % SLOTS;
+        const int phase = k / SLOTS;
+        ++k;
+        const bool ok = whole_warp ? c.wait_warp(FULL + slot, phase) : c.wait(FULL + slot, phase);
+        if (!ok) return -1;
+        const int u = c.ring[slot];
+        if (whole_warp) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(c.bar(EMPTY + slot));
+        } else {
+            mbar_arrive(c.bar(EMPTY + slot));
+        }
+        return u;
+    }
 };
 
 // ----------------------------------------------------------- TMA producer
@@ -197,11 +224,33 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
     const uint64_t pol_kv = policy_evict_last();
     int kv_idx = 0, qit = 0;
     bool ok = true;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
-        const int u = unit_of_round(round);
-        if (u >= p.num_units) continue;
+    // Claims the CTA's next unit from the global counter and publishes it in
+    // the ring (-1 once the units are used up).
+    int claimed = 0;
+    auto claim = [&]() -> int {
+        const int slot = claimed % C::UNIT_SLOTS;
+        if (claimed >= C::UNIT_SLOTS && !c.wait(C::UNIT_EMPTY + slot, claimed / C::UNIT_SLOTS - 1)) return -2;
+        int v = atomicAdd(p.sched, 1);
+        if (v >= p.num_units) v = -1;
+        c.ring[slot] = v;
+        mbar_arrive(c.bar(C::UNIT_FULL + slot));
+        ++claimed;
+        return v;
+    };
+    int u = claim();
+    while (u >= 0 && ok) {
+        // The following unit is claimed one ahead, so that its Q tiles can be
+        // pulled into L2 while this unit runs.
+        const int u_next = claim();
+        if (u_next == -2) {
+            ok = false;
+            break;
+        }
         const Unit U = unit_info<CAUSAL>(u, p);
-        if (U.nmax == 0) continue;
+        if (U.nmax == 0) {
+            u = u_next;
+            continue;
+        }
         const int qb = qit % C::QB;
         if (qit >= C::QB && !c.wait(C::Q_EMPTY + qb, qit / C::QB - 1)) {
             ok = false;
@@ -220,9 +269,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
             // One Q buffer: the next unit's Q tiles can only be loaded once
             // this unit's last Q K^T product is done. Pull them into L2 now so
             // that load does not wait on HBM.
-            const int un = unit_of_round(round + 1);
-            if (un < p.num_units) {
-                const Unit N = unit_info<CAUSAL>(un, p);
+            if (u_next >= 0) {
+                const Unit N = unit_info<CAUSAL>(u_next, p);
                 for (int t = 0; t < 2; ++t) {
                     if ((t ? N.n1 : N.n0) == 0) continue;
                     for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(mq, pn * 64, N.q0 + 128 * t, N.bh);
@@ -245,6 +293,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
                 ++kv_idx;
             }
         }
+        u = u_next;
     }
     // Every copy issued must land before this CTA's shared memory is
     // released: wait for the last fill of each stage and of each Q buffer.
@@ -274,9 +323,10 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
     int pv_cnt[2] = {0, 0};   // P V products issued per query tile
     int units_o[2] = {0, 0};  // units whose last product was committed, per tile
     bool ok = true;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
-        const int u = unit_of_round(round);
-        if (u >= p.num_units) continue;
+    UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
+    while (ok) {
+        const int u = units.next(c, false);
+        if (u < 0) break;
         const Unit U = unit_info<CAUSAL>(u, p);
         if (U.nmax == 0) continue;
         const int qb = qit % C::QB;
@@ -366,9 +416,10 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
     const uint64_t c2 = f2_pack(cl2, cl2);
     int s_cnt = 0, st_cnt = 0;
     bool ok = true;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
-        const int u = unit_of_round(round);
-        if (u >= p.num_units) continue;
+    UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
+    while (ok) {
+        const int u = units.next(c, true);
+        if (u < 0) break;
         const Unit U = unit_info<CAUSAL>(u, p);
         const int ntile = t ? U.n1 : U.n0;
         if (ntile == 0) continue;
@@ -520,9 +571,10 @@ __device__ __forceinline__ void epilogue_role(const Bf16Params& p, const Ctx& c)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
     bool ok = true;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.num_units && ok; ++round) {
-        const int u = unit_of_round(round);
-        if (u >= p.num_units) continue;
+    UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
+    while (ok) {
+        const int u = units.next(c, true);
+        if (u < 0) break;
         const Unit U = unit_info<CAUSAL>(u, p);
         // Epilogue: O = acc / l in bf16, LSE = ln2 * (m + log2 l).
 #pragma unroll
@@ -631,6 +683,7 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     c.stats_sm = reinterpret_cast<float*>(smem + C::STATS_OFF);
     c.abort = &abort_sh;
     c.err = p.err;
+    c.ring = reinterpret_cast<volatile int*>(smem + C::RING_OFF);
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
@@ -651,6 +704,10 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             mbar_init(c.bar(C::ST_EMPTY + t), 128);
         }
         mbar_init(c.bar(C::DRAIN), 1);
+        for (int s = 0; s < C::UNIT_SLOTS; ++s) {
+            mbar_init(c.bar(C::UNIT_FULL + s), 1);
+            mbar_init(c.bar(C::UNIT_EMPTY + s), C::UNIT_READERS);
+        }
         fence_barrier_init();
     }
     if (warp == 13) {
@@ -690,6 +747,15 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
     if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(c.tmem, C::TMEM_COLS);
+    }
+    // The last CTA to finish resets the unit counter for the next launch that
+    // uses it; every CTA's claims precede its count here.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 1, 0);
+        }
     }
 }
 

@@ -26,6 +26,9 @@ struct Bf16Params {
     float* ws_lse;       // splits > 1: [splits, BH, M] fp32 partial log-sum-exps
     int heads_per_group; // causal tile order: heads that share a group
     float scale_log2;    // scale * log2(e)
+    int* sched;          // [2]: next unit to claim, CTAs finished. Zero when the
+                         // launch starts; the launch's last CTA sets both back
+                         // to zero, so a slot serves one running launch at a time.
 };
 
 // Launches the bf16 kernel for head dimension D (64, 96 or 128); the three

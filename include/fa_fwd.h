@@ -40,9 +40,13 @@
  * synchronise; the results are ready when the stream reaches them.
  *
  * The library allocates nothing per call. On its first call on a device it
- * allocates one 4-byte device status word for that device, which it keeps
- * until the process exits; device-side failures (a pipeline wait that ran
- * out of time) are OR-ed into that word and read by fa_get_device_status().
+ * allocates one small block of device state for that device (520 bytes),
+ * which it keeps until the process exits: a status word, into which
+ * device-side failures (a pipeline wait that ran out of time) are OR-ed and
+ * which fa_get_device_status() reads, and 64 pairs of work counters that
+ * the bf16 kernel's CTAs use to claim work units. Each bf16 launch takes the
+ * next pair in turn and leaves it at zero when it ends, so at most 64 bf16
+ * launches (fa_fwd, fa_fwd_splitkv) may be running on a device at once.
  *
  * Errors
  * ------
@@ -157,21 +161,21 @@ fa_status fa_get_device_status(void* stream);
  * pages have no counterpart to this entry point; it exists for the library's
  * users.
  *
- * Who needs it: fa_fwd cudaMallocs a 4-byte status word on its first call on
- * each device. Applications whose caching allocator or memory pool owns all
+ * Who needs it: fa_fwd cudaMallocs a small block of device state (its status
+ * word and work counters) on its first call on each device. Applications whose caching allocator or memory pool owns all
  * device memory, serving loops that must avoid the implicit device-wide
  * synchronisation a cudaMalloc can cause, and processes under a fixed
  * device-memory quota cannot allow that. This entry point calls no
  * cudaMalloc, cudaFree or other allocating routine: the kernel's scratch (its
- * status word) lives in a file-scope static device array of 64 32-bit words
- * (256 bytes), which every GPU that loads the library holds until the
- * process exits. No problem size needs more than that one word; a kernel
- * needing more than the array holds would be rejected with
- * FA_ERR_UNSUPPORTED.
+ * status word and the two counters its CTAs claim work units from) lives in
+ * a file-scope static device array of 64 32-bit words (256 bytes), which
+ * every GPU that loads the library holds until the process exits. No
+ * problem size needs more than those three words; a kernel needing more
+ * than the array holds would be rejected with FA_ERR_UNSUPPORTED.
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture. Every call clears the scratch word on
+ * first call before any stream capture. Every call clears the scratch words on
  * `stream` before its launch. All calls share the one array, so calls that
  * overlap on the GPU (other streams, other host threads) race on it. A
  * device-side pipeline timeout in this variant leaves O and LSE undefined

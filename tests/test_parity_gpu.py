@@ -162,6 +162,41 @@ def test_bf16_deterministic_and_stream():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
+def test_bf16_back_to_back_launches_on_two_streams():
+    """The bf16 kernel's CTAs claim work units from a counter that each launch
+    takes from a ring of 64 and leaves at zero when it ends. 70 launches of
+    each of two problems, alternating between two streams that run at the
+    same time, wrap the ring; every launch must give the same bits as the
+    first, and the first must match the oracle."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from parity import to_device_bf16
+
+    probs = []
+    for i, (B, H, M, N, D, causal) in enumerate([(1, 4, 600, 600, 128, True), (2, 2, 300, 700, 64, False)]):
+        q, k, v = (_rand((B, H, S, D), 40 + 3 * i + j) for j, S in enumerate((M, N, N)))
+        probs.append((q, k, v, D ** -0.5, causal, tuple(to_device_bf16(x) for x in (q, k, v))))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for _ in range(70):
+        for i, (q, k, v, scale, causal, (tq, tk, tv)) in enumerate(probs):
+            with torch.cuda.stream(streams[i]):
+                o = torch.empty_like(tq)
+                lse = torch.empty(tq.shape[:-1], dtype=torch.float32, device="cuda")
+                fa.fa_fwd(tq, tk, tv, o, lse, scale, causal)
+                outs[i].append((o, lse))
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for i, (q, k, v, scale, causal, _) in enumerate(probs):
+        o0, l0 = outs[i][0]
+        for o, lse in outs[i][1:]:
+            assert torch.equal(o, o0) and torch.equal(lse, l0)
+        o_ref, lse_ref = attention(q, k, v, scale, causal)
+        check_bf16(o0.float().cpu().numpy(), l0.cpu().numpy(), o_ref, lse_ref, f"problem {i}")
+
+
 # ------------------------------------------------ full-size workloads (sampled)
 
 def _full_size_check(w, heads, rows_per_head):
