@@ -313,15 +313,33 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
     using C = Bf16Cfg<D>;
     constexpr uint32_t id_s = idesc_bf16_f32(128, C::BN, false);
     constexpr uint32_t id_o = idesc_bf16_f32(128, D, true);
+    constexpr uint32_t kPanel = C::PANEL_BYTES >> 4;
     const uint32_t sq = smem_u32(c.sQ);
     const uint32_t skv = smem_u32(c.sKV);
     // Descriptor templates with a zero start address; adding (address >> 4)
     // fills the 14-bit start field (shared addresses are < 256 KB).
     const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);
     const uint64_t desc_v = smem_desc_sw128(0, C::PANEL_BYTES, 1024);
+    // S_t = Q_t K^T: Q and K tiles K-major, 128-byte swizzle; a 16-column
+    // K-step advances 32 B inside a 64-column panel, 4 steps a panel.
+    auto issue_s = [&](uint32_t s_col, uint64_t dq, uint64_t dk) {
+#pragma unroll
+        for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+            mma_ss(c.tmem + s_col, dq + off, dk + off, id_s, kk > 0 ? 1u : 0u);
+        }
+    };
+    // O_t (+)= P_t V: P from tensor memory (aliasing S_t), V MN-major with
+    // 128-byte swizzle (LBO = the 64-column panel stride, SBO = 8 rows of
+    // 128 B); 16 keys per step. The first product of a unit overwrites O_t.
+    auto issue_pv = [&](uint32_t o_col, uint32_t s_col, uint64_t dv, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < C::PV_STEPS; ++kk)
+            mma_ts(c.tmem + o_col, c.tmem + s_col + kk * 8, dv + kk * (2048 >> 4), id_o, (first && kk == 0) ? 0u : 1u);
+    };
     int kv_idx = 0, qit = 0;
-    int pv_cnt[2] = {0, 0};   // P V products issued per query tile
-    int units_o[2] = {0, 0};  // units whose last product was committed, per tile
+    int pv0 = 0, pv1 = 0;   // P V products issued per query tile
+    int uo0 = 0, uo1 = 0;   // units whose last product was committed, per tile
     bool ok = true;
     UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
     while (ok) {
@@ -329,73 +347,76 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
         if (u < 0) break;
         const Unit U = unit_info<CAUSAL>(u, p);
         if (U.nmax == 0) continue;
+        const int n0 = U.n0, n1 = U.n1, nm = U.nmax;
         const int qb = qit % C::QB;
         if (!c.wait(C::Q_FULL + qb, qit / C::QB)) {
             ok = false;
             break;
         }
         tc_fence_after();
-        for (int j = 0; j <= U.nmax && ok; ++j) {
-            const int kidx = kv_idx + 2 * j, vidx = kv_idx + 2 * j - 1;
-            const int kst = kidx % C::NS, vst = (vidx + C::NS) % C::NS;
+        const uint64_t dq0 = desc_k + ((sq + (qb * 2 + 0) * C::TILE_BYTES) >> 4);
+        const uint64_t dq1 = desc_k + ((sq + (qb * 2 + 1) * C::TILE_BYTES) >> 4);
+        // Key tile j: K(j) sits in ring slot kidx = kv_idx + 2j, V(j-1) in
+        // slot kidx - 1.
+        for (int j = 0; j <= nm; ++j) {
+            const int kidx = kv_idx + 2 * j;
+            const int kst = kidx % C::NS, vst = (kidx + C::NS - 1) % C::NS;
+            const uint64_t dk = desc_k + ((skv + kst * C::TILE_BYTES) >> 4);
+            const uint64_t dv = desc_v + ((skv + vst * C::TILE_BYTES) >> 4);
             // V(j-1) gates the P V products, K(j) only the Q K^T ones.
-            if (j >= 1 && !c.wait(C::KV_FULL + vst, vidx / C::NS)) ok = false;
-            bool k_ready = false;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int nt = t ? U.n1 : U.n0;
-                const uint32_t s_col = t ? C::S_COL1 : C::S_COL0;
-                const uint32_t o_col = t ? C::O_COL1 : C::O_COL0;
-                if (ok && j >= 1 && j - 1 < nt) {
-                    ok = c.wait(C::P_FULL + t, pv_cnt[t]);
-                    // The first product of a unit overwrites O_t: the
-                    // previous unit's epilogue must have read it.
-                    if (ok && j == 1 && units_o[t] > 0) ok = c.wait(C::O_FREE + t, units_o[t] - 1);
-                    if (ok) {
-                        tc_fence_after();
-                        // V tile: MN-major, 128-byte swizzle; LBO = the
-                        // 64-column panel stride, SBO = 8 rows of 128 B.
-                        const uint64_t dv = desc_v + ((skv + vst * C::TILE_BYTES) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < C::PV_STEPS; ++kk)
-                            mma_ts(c.tmem + o_col, c.tmem + s_col + kk * 8, dv + kk * (2048 >> 4), id_o,
-                                   (j > 1 || kk > 0) ? 1u : 0u);
-                        ++pv_cnt[t];
-                        if (j == nt) {
-                            mma_commit(c.bar(C::O_DONE + t));
-                            ++units_o[t];
-                        }
-                        // V(j-1) is free once its last product completes
-                        // (a commit covers every MMA issued before it).
-                        // Tile 1 is issued after tile 0, so it is V's last
-                        // user whenever it uses V(j-1) at all.
-                        if (t == 1 || j - 1 >= U.n1) mma_commit(c.bar(C::KV_EMPTY + vst));
-                    }
-                }
-                if (ok && j < nt && !k_ready) {
-                    ok = c.wait(C::KV_FULL + kst, kidx / C::NS);
-                    k_ready = ok;
-                    tc_fence_after();
-                }
-                if (ok && j < nt) {
-                    // Q and K tiles: K-major, 128-byte swizzle; a 16-column
-                    // K-step advances 32 B inside a panel, 4 steps a panel.
-                    const uint64_t dq = desc_k + ((sq + (qb * 2 + t) * C::TILE_BYTES) >> 4);
-                    const uint64_t dk = desc_k + ((skv + kst * C::TILE_BYTES) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                        constexpr uint32_t kPanel = C::PANEL_BYTES >> 4;
-                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
-                        mma_ss(c.tmem + s_col, dq + off, dk + off, id_s, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(c.bar(C::S_FULL + t));
-                }
+            if (j >= 1 && !c.wait(C::KV_FULL + vst, (kidx - 1) / C::NS)) {
+                ok = false;
+                break;
             }
-            if (!ok) break;
-            if (j < U.nmax) mma_commit(c.bar(C::KV_EMPTY + kst));
-            if (j == U.nmax - 1) mma_commit(c.bar(C::Q_EMPTY + qb));
+            if (j >= 1 && j <= n0) {
+                if (!c.wait(C::P_FULL + 0, pv0) || (j == 1 && uo0 > 0 && !c.wait(C::O_FREE + 0, uo0 - 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(C::O_COL0, C::S_COL0, dv, j == 1);
+                ++pv0;
+                if (j == n0) {
+                    mma_commit(c.bar(C::O_DONE + 0));
+                    ++uo0;
+                }
+                // V(j-1) is free once its last product completes (a commit
+                // covers every MMA issued before it); tile 1, issued after
+                // tile 0, is its last user whenever it uses it at all.
+                if (j > n1) mma_commit(c.bar(C::KV_EMPTY + vst));
+            }
+            if (j < nm && !c.wait(C::KV_FULL + kst, kidx / C::NS)) {
+                ok = false;
+                break;
+            }
+            if (j < n0) {
+                tc_fence_after();
+                issue_s(C::S_COL0, dq0, dk);
+                mma_commit(c.bar(C::S_FULL + 0));
+            }
+            if (j >= 1 && j <= n1) {
+                if (!c.wait(C::P_FULL + 1, pv1) || (j == 1 && uo1 > 0 && !c.wait(C::O_FREE + 1, uo1 - 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_pv(C::O_COL1, C::S_COL1, dv, j == 1);
+                ++pv1;
+                if (j == n1) {
+                    mma_commit(c.bar(C::O_DONE + 1));
+                    ++uo1;
+                }
+                mma_commit(c.bar(C::KV_EMPTY + vst));
+            }
+            if (j < n1) {
+                tc_fence_after();
+                issue_s(C::S_COL1, dq1, dk);
+                mma_commit(c.bar(C::S_FULL + 1));
+            }
+            if (j < nm) mma_commit(c.bar(C::KV_EMPTY + kst));
+            if (j == nm - 1) mma_commit(c.bar(C::Q_EMPTY + qb));
         }
-        kv_idx += 2 * U.nmax;
+        kv_idx += 2 * nm;
         ++qit;
     }
     // All MMAs issued must finish before tensor memory is freed.
