@@ -224,13 +224,15 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
     const uint64_t pol_kv = policy_evict_last();
     int kv_idx = 0, qit = 0;
     bool ok = true;
-    // Claims the CTA's next unit from the global counter and publishes it in
-    // the ring (-1 once the units are used up).
+    // Claims the CTA's next unit and publishes it in the ring (-1 once the
+    // units are used up). A CTA's first unit is its own index (the grid
+    // never has more CTAs than units); the rest come from the global
+    // counter, which numbers the units after the first gridDim.x.
     int claimed = 0;
     auto claim = [&]() -> int {
         const int slot = claimed % C::UNIT_SLOTS;
         if (claimed >= C::UNIT_SLOTS && !c.wait(C::UNIT_EMPTY + slot, claimed / C::UNIT_SLOTS - 1)) return -2;
-        int v = atomicAdd(p.sched, 1);
+        int v = (claimed == 0) ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
         if (v >= p.num_units) v = -1;
         c.ring[slot] = v;
         mbar_arrive(c.bar(C::UNIT_FULL + slot));
