@@ -125,6 +125,40 @@ class ClockSampler:
         return summarize_clocks(rows)
 
 
+# Sources of the bf16 kernel; a recorded ncu traffic figure is reported only
+# while these hash to the value it was taken with.
+KERNEL_SOURCES = ["fa_bf16_kernel.cuh", "ptx.cuh", "fa_internal.h", "fa_api.cu",
+                  "fa_bf16_d64.cu", "fa_bf16_d96.cu", "fa_bf16_d128.cu"]
+TRAFFIC_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
+                            "fa_fwd_bf16_dram_traffic.json")
+
+
+def kernel_sources_sha() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "flashattention_fa_fwd_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes (read + written) of one launch of the bf16 kernel on this
+    workload, from the ncu capture recorded under profiles/, or None when
+    there is none or the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        if rec.get("kernel_sha") != kernel_sources_sha():
+            return None
+        e = rec["workloads"].get(workload)
+        return None if e is None else int(e["dram_bytes_read"]) + int(e["dram_bytes_write"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def summarize_clocks(rows):
     """Median SM clock, max clock and the throttle reasons seen (any sample)."""
     def num(x):
@@ -404,7 +438,8 @@ def gpu_arm(args, w, rank, world, local_rank):
                        if in_bytes > 129e6 else "inputs fit in L2 (warm)"),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 else None,
                      "peak_source": f"{peaks.get('source')} bf16_tflops (burst); sustained "
                                     f"{peaks.get('bf16_tflops_sustained')}",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
