@@ -108,6 +108,26 @@ def test_bf16_large_logits_many_tiles():
     check_bf16(o, lse, o_ref, lse_ref, "rising max")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_row_max_jumps_between_key_tiles(causal):
+    """Rows whose max jumps in a later key tile, by less than 2^8, by 2^9 to
+    2^32 (weights far above 1 against the row's stale reference) and by more
+    than 2^32 (the tile is redone against its own max): one direction of Q
+    is scaled per row, the same direction of K per key tile."""
+    B, H, M, N, D = 1, 2, 384, 640, 64
+    q = _rand((B, H, M, D), 71, 0.3)
+    k = _rand((B, H, N, D), 72, 0.3)
+    v = _rand((B, H, N, D), 73)
+    row_gain = np.array([0.0, 0.5, 1.0, 2.0, 4.0, 8.0], dtype=np.float32)[np.arange(M) % 6]
+    tile_gain = np.array([0.0, 3.0, 0.5, 12.0, 40.0], dtype=np.float32)[np.arange(N) // 128]
+    q[..., 0] = round_to_bf16(q[..., 0] + row_gain)
+    k[..., 0] = round_to_bf16(k[..., 0] + tile_gain)
+    scale = D ** -0.5
+    o, lse = run_bf16(q, k, v, scale, causal)
+    o_ref, lse_ref = attention(q, k, v, scale, causal)
+    check_bf16(o, lse, o_ref, lse_ref, f"max jumps (causal={causal})")
+
+
 def test_bf16_worked_example_padded():
     """The worked example embedded in D = 64 (other features zero): output
     25.752; the bound is the bf16 rounding of p (2^-9 relative) times |V| = 30
