@@ -25,7 +25,8 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
-            "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest")
+            "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest",
+            "fa_fwd_host", "fa_fwd_host_workspace_bytes")
 
 
 class FaError(RuntimeError):
@@ -66,6 +67,11 @@ def load_library():
         lib.fa_fwd_splitkv_workspace_bytes.restype = i64
         lib.fa_fwd_splitkv_suggest.argtypes = [i64, i64, i64, i64, ctypes.c_int]
         lib.fa_fwd_splitkv_suggest.restype = ctypes.c_int
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                    i64, vp, i64, vp]
+        lib.fa_fwd_host.restype = ctypes.c_int
+        lib.fa_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
+        lib.fa_fwd_host_workspace_bytes.restype = i64
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = ctypes.c_int
         lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -111,6 +117,18 @@ def fa_fwd_splitkv_workspace_bytes(B: int, H: int, M: int, D: int, num_splits: i
 
 def fa_fwd_splitkv_suggest(B: int, H: int, M: int, N: int, causal: bool) -> int:
     return load_library().fa_fwd_splitkv_suggest(B, H, M, N, int(bool(causal)))
+
+
+def fa_fwd_host_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+                    scale: float, causal: bool, heads_per_chunk: int, workspace: int, workspace_bytes: int,
+                    stream: int = 0) -> int:
+    """Calls fa_fwd_host with raw host addresses and a device workspace; returns the status."""
+    return load_library().fa_fwd_host(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)),
+                                      int(heads_per_chunk), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, M: int, N: int, D: int, heads_per_chunk: int = 0) -> int:
+    return load_library().fa_fwd_host_workspace_bytes(B, H, M, N, D, heads_per_chunk)
 
 
 def fa_status_string(status: int) -> str:
@@ -245,3 +263,43 @@ def fa_get_device_status(stream=None, device=None) -> int:
         s = torch.cuda.current_stream(dev).cuda_stream if stream is None else (
             stream if isinstance(stream, int) else stream.cuda_stream)
         return load_library().fa_get_device_status(s)
+
+
+def fa_fwd_host(q, k, v, o, lse, scale: float, causal: bool = False, heads_per_chunk: int = 0,
+                workspace=None, device=None, stream=None) -> None:
+    """bf16 attention forward on host tensors, copies overlapped with compute.
+
+    q, k, v, o, lse as in :func:`fa_fwd` but contiguous CPU tensors (pinned
+    for the copies to overlap). ``workspace`` is a CUDA uint8 tensor of at
+    least fa_fwd_host_workspace_bytes(...) bytes (allocated here with torch
+    when None) on ``device`` (default: the current device). Asynchronous on
+    ``stream`` (default: that device's current torch stream): synchronise it
+    before reading o and lse.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bfloat16 torch.Tensor")
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    if lse.dtype != torch.float32 or lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 CPU tensor")
+    B, H, M, D = _shape4(q, "q")
+    Bk, Hk, N, Dk = _shape4(k, "k")
+    if (Bk, Hk, Dk) != (B, H, D) or _shape4(v, "v") != (B, H, N, D) or _shape4(o, "o") != (B, H, M, D):
+        raise ValueError("k, v must be [B, H, N, D] and o [B, H, M, D], matching q")
+    if lse.numel() != B * H * M:
+        raise ValueError("lse must hold B*H*M values")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        need = fa_fwd_host_workspace_bytes(B, H, M, N, D, heads_per_chunk)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        s = torch.cuda.current_stream(dev).cuda_stream if stream is None else (
+            stream if isinstance(stream, int) else stream.cuda_stream)
+        st = fa_fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             B, H, M, N, D, scale, causal, heads_per_chunk, workspace.data_ptr(),
+                             workspace.numel(), s)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_host")

@@ -160,6 +160,15 @@ constexpr double kLog2e = 1.4426950408889634;
 
 }  // namespace
 
+namespace {
+
+// The bf16 forward on device buffers whose arguments have been checked:
+// tensor maps, parameters and the launch on `s`.
+fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t bh,
+                             int64_t M, int64_t N, int64_t D, float scale, int causal, cudaStream_t s);
+
+}  // namespace
+
 FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
                         int64_t M, int64_t N, int64_t D, float scale, int causal, void* stream) {
     bool empty = false;
@@ -168,7 +177,14 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     if (D != 64 && D != 96 && D != 128)
         return fail(FA_ERR_UNSUPPORTED, "bf16 fa_fwd supports D in {64, 96, 128} (got %lld)", (long long)D);
     if (empty) return FA_OK;
-    const int64_t bh = B * H;
+    return launch_fwd_checked(q, k, v, o, lse, B * H, M, N, D, scale, causal, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* o, float* lse, int64_t bh,
+                             int64_t M, int64_t N, int64_t D, float scale, int causal, cudaStream_t s) {
+    fa_status st;
     const int64_t n_pairs = (M + 255) / 256;
     if (bh * n_pairs > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many query tiles for one launch");
     uint32_t* word = nullptr;
@@ -200,7 +216,6 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     p.sched = sched;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
         case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
@@ -210,6 +225,8 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
     if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
     return FA_OK;
 }
+
+}  // namespace
 
 FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int64_t B,
                             int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal, void* stream) {
@@ -497,5 +514,163 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
         default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
+    return FA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// fa_fwd_host: the bf16 forward on host buffers, with the copies overlapped.
+//
+// The heads (b, h) are processed in chunks of `heads_per_chunk` through two
+// slots of a caller-provided device workspace. Two library-owned streams per
+// device carry the copies: chunk c's Q, K, V go host -> device on the first
+// while the kernel runs chunk c - 1 on the caller's stream and chunk c - 2's
+// O and LSE go device -> host on the second. Events order a slot's reuse:
+// its inputs are overwritten only after the kernel that read them, its
+// outputs only after they were copied out. The call is asynchronous on the
+// caller's stream: the auxiliary streams first wait for an event recorded
+// on it, and it finally waits for the last copy.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kHostSlots = 2;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in_ready[kHostSlots] = {}, comp_done[kHostSlots] = {}, out_done[kHostSlots] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+struct SlotLayout {
+    int64_t q, k, v, o, lse, bytes;   // offsets within a slot, slot size
+};
+
+SlotLayout slot_layout(int64_t hc, int64_t M, int64_t N, int64_t D) {
+    SlotLayout L;
+    L.q = 0;
+    L.k = L.q + align256(hc * M * D * 2);
+    L.v = L.k + align256(hc * N * D * 2);
+    L.o = L.v + align256(hc * N * D * 2);
+    L.lse = L.o + align256(hc * M * D * 2);
+    L.bytes = L.lse + align256(hc * M * 4);
+    return L;
+}
+
+int64_t default_chunk(int64_t bh) { return bh < 8 ? bh : (bh + 7) / 8; }
+
+fa_status pipe_setup(int dev, HostPipe** out) {
+    HostPipe& P = g_pipe[dev];
+    if (!P.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&P.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&P.end, cudaEventDisableTiming);
+        for (int s = 0; s < kHostSlots && e == cudaSuccess; ++s) {
+            e = cudaEventCreateWithFlags(&P.in_ready[s], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&P.comp_done[s], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&P.out_done[s], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "creating the copy streams and events");
+        P.ready = true;
+    }
+    *out = &P;
+    return FA_OK;
+}
+
+}  // namespace
+
+FA_API int64_t fa_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                                           int64_t heads_per_chunk) {
+    if (B < 0 || H < 0 || M < 0 || N < 0 || D < 1 || heads_per_chunk < 0) return -1;
+    const int64_t bh = B * H;
+    if (bh == 0 || M == 0) return 0;
+    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh) : heads_per_chunk;
+    if (hc > bh) hc = bh;
+    return kHostSlots * slot_layout(hc, M, N, D).bytes;
+}
+
+FA_API fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                             int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal,
+                             int64_t heads_per_chunk, void* workspace, int64_t workspace_bytes, void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 2, &empty);
+    if (st != FA_OK) return st;
+    if (D != 64 && D != 96 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "bf16 fa_fwd_host supports D in {64, 96, 128} (got %lld)", (long long)D);
+    if (heads_per_chunk < 0) return fail(FA_ERR_INVALID_ARG, "heads_per_chunk must be >= 0");
+    if (empty) return FA_OK;
+    const int64_t bh = B * H;
+    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh) : heads_per_chunk;
+    if (hc > bh) hc = bh;
+    const SlotLayout L = slot_layout(hc, M, N, D);
+    if (workspace == nullptr || workspace_bytes < kHostSlots * L.bytes)
+        return fail(FA_ERR_INVALID_ARG, "workspace of %lld bytes needed (got %lld)",
+                    (long long)(kHostSlots * L.bytes), (long long)workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(FA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    // Whole calls are enqueued one at a time, so that each call's waits
+    // refer to its own event records.
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* P = nullptr;
+    if ((st = pipe_setup(dev, &P)) != FA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto check = [&](cudaError_t err, const char* what) -> bool {
+        if (err != cudaSuccess) {
+            cuda_fail(err, what);
+            return false;
+        }
+        return true;
+    };
+    if (!check(cudaEventRecord(P->start, s), "cudaEventRecord") ||
+        !check(cudaStreamWaitEvent(P->in, P->start, 0), "cudaStreamWaitEvent") ||
+        !check(cudaStreamWaitEvent(P->out, P->start, 0), "cudaStreamWaitEvent"))
+        return FA_ERR_CUDA;
+    const uint8_t* hq = static_cast<const uint8_t*>(q);
+    const uint8_t* hk = static_cast<const uint8_t*>(k);
+    const uint8_t* hv = static_cast<const uint8_t*>(v);
+    uint8_t* ho = static_cast<uint8_t*>(o);
+    uint8_t* hl = reinterpret_cast<uint8_t*>(lse);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t qrow = M * D * 2, krow = N * D * 2, lrow = M * 4;   // bytes per head
+    int64_t chunk = 0;
+    for (int64_t h0 = 0; h0 < bh; h0 += hc, ++chunk) {
+        const int64_t n = (bh - h0 < hc) ? bh - h0 : hc;
+        const int slot = static_cast<int>(chunk % kHostSlots);
+        uint8_t* base = ws + slot * L.bytes;
+        // inputs: the slot's previous kernel must have read them
+        if (chunk >= kHostSlots && !check(cudaStreamWaitEvent(P->in, P->comp_done[slot], 0), "cudaStreamWaitEvent"))
+            return FA_ERR_CUDA;
+        if (!check(cudaMemcpyAsync(base + L.q, hq + h0 * qrow, n * qrow, cudaMemcpyHostToDevice, P->in), "copying q") ||
+            (N > 0 && !check(cudaMemcpyAsync(base + L.k, hk + h0 * krow, n * krow, cudaMemcpyHostToDevice, P->in),
+                             "copying k")) ||
+            (N > 0 && !check(cudaMemcpyAsync(base + L.v, hv + h0 * krow, n * krow, cudaMemcpyHostToDevice, P->in),
+                             "copying v")) ||
+            !check(cudaEventRecord(P->in_ready[slot], P->in), "cudaEventRecord"))
+            return FA_ERR_CUDA;
+        // kernel: inputs landed, and the slot's previous outputs were copied out
+        if (!check(cudaStreamWaitEvent(s, P->in_ready[slot], 0), "cudaStreamWaitEvent") ||
+            (chunk >= kHostSlots && !check(cudaStreamWaitEvent(s, P->out_done[slot], 0), "cudaStreamWaitEvent")))
+            return FA_ERR_CUDA;
+        st = launch_fwd_checked(base + L.q, base + L.k, base + L.v, base + L.o,
+                                reinterpret_cast<float*>(base + L.lse), n, M, N, D, scale, causal, s);
+        if (st != FA_OK) return st;
+        if (!check(cudaEventRecord(P->comp_done[slot], s), "cudaEventRecord") ||
+            !check(cudaStreamWaitEvent(P->out, P->comp_done[slot], 0), "cudaStreamWaitEvent") ||
+            !check(cudaMemcpyAsync(ho + h0 * qrow, base + L.o, n * qrow, cudaMemcpyDeviceToHost, P->out), "copying o") ||
+            !check(cudaMemcpyAsync(hl + h0 * lrow, base + L.lse, n * lrow, cudaMemcpyDeviceToHost, P->out),
+                   "copying lse") ||
+            !check(cudaEventRecord(P->out_done[slot], P->out), "cudaEventRecord"))
+            return FA_ERR_CUDA;
+    }
+    if (!check(cudaEventRecord(P->end, P->out), "cudaEventRecord") ||
+        !check(cudaStreamWaitEvent(s, P->end, 0), "cudaStreamWaitEvent"))
+        return FA_ERR_CUDA;
     return FA_OK;
 }

@@ -148,6 +148,47 @@ int64_t fa_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t 
 int fa_fwd_splitkv_suggest(int64_t B, int64_t H, int64_t M, int64_t N, int causal);
 
 /*
+ * bf16 forward on HOST buffers: the result of fa_fwd (same layouts, checks
+ * and results) for q, k, v, o and lse in host memory, with the host <-> device
+ * copies overlapped with the computation. It is how the library is used when
+ * the tensors live on the host; the pages' statement of the problem ("FlashAttention
+ * in Triton: A Tile-by-Tile Walkthrough", section "Full Triton implementation":
+ * `solve` writes a preallocated output) does not say where they live.
+ *
+ * The B*H heads are processed in chunks of `heads_per_chunk` (0 = the
+ * library's choice: about an eighth of them) through two slots of a
+ * caller-owned device workspace: while the kernel runs one chunk on
+ * `stream`, the next chunk's q, k, v are copied in and the previous chunk's
+ * o, lse copied out on two streams the library creates once per device.
+ *
+ *   q, k, v, o, lse  host memory, 16-byte aligned (lse 4); page-locked
+ *                    (cudaHostAlloc / pinned) for the copies to overlap --
+ *                    pageable memory works, with the driver's synchronous
+ *                    staging
+ *   heads_per_chunk  >= 0
+ *   workspace        device memory owned by the caller, 256-byte aligned, at
+ *                    least fa_fwd_host_workspace_bytes(...) bytes
+ *
+ * Asynchronous on `stream`: the host buffers must stay valid and unchanged,
+ * and o and lse are only complete, once the stream reaches the point of the
+ * call (e.g. after cudaStreamSynchronize(stream)). Calls that may run at the
+ * same time on different streams need different workspaces. Errors as
+ * fa_fwd, plus FA_ERR_INVALID_ARG for a negative heads_per_chunk or a
+ * missing, short or misaligned workspace, and FA_ERR_CUDA if creating the
+ * library's streams or events, or enqueueing a copy, fails.
+ */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                      float scale, int causal, int64_t heads_per_chunk,
+                      void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Device workspace bytes fa_fwd_host needs: two slots, each holding one
+ * chunk's q, k, v, o (bf16) and lse (fp32), every array padded to 256 bytes
+ * (0 for an empty problem; -1 for invalid arguments). Needs no GPU. */
+int64_t fa_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                                    int64_t heads_per_chunk);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns FA_ERR_TIMEOUT if a kernel launched since the last call gave
  * up on a pipeline wait (its outputs are then undefined), FA_ERR_CUDA if the

@@ -123,3 +123,26 @@ def test_splitkv_workspace_size_and_checks(lib):
     assert fa.fa_fwd_splitkv_raw(*args, 17, W, need, 0) == fa.FA_ERR_INVALID_ARG         # too many splits
     assert fa.fa_fwd_splitkv_raw(A, 2 * A, 3 * A, 4 * A, 5 * A, 0, 2, 256, 512, 64, 0.125, False,
                                  2, W, need, 0) == fa.FA_OK                                # empty problem
+
+
+def test_host_entry_workspace_size_and_checks(lib):
+    # two slots; per slot q, k, v, o (bf16) and lse (fp32), each padded to 256 bytes
+    def pad(x):
+        return (x + 255) // 256 * 256
+    hc, M, N, D = 3, 100, 300, 64
+    slot = pad(hc * M * D * 2) + 2 * pad(hc * N * D * 2) + pad(hc * M * D * 2) + pad(hc * M * 4)
+    assert fa.fa_fwd_host_workspace_bytes(2, 4, M, N, D, hc) == 2 * slot
+    # default chunk: an eighth of the heads (rounded up); never more heads than exist
+    assert fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 0) == fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 32)
+    assert fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, 50) == fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, 2)
+    assert fa.fa_fwd_host_workspace_bytes(0, 2, M, N, D, 0) == 0
+    assert fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, -1) == -1
+    need = fa.fa_fwd_host_workspace_bytes(1, 2, 256, 512, 64, 0)
+    W = 64 * A
+    args = (*PTRS, 1, 2, 256, 512, 64, 0.125, False)
+    assert fa.fa_fwd_host_raw(*args, 0, W, need - 256, 0) == fa.FA_ERR_INVALID_ARG   # too small
+    assert fa.fa_fwd_host_raw(*args, 0, 0, need, 0) == fa.FA_ERR_INVALID_ARG          # missing
+    assert fa.fa_fwd_host_raw(*args, 0, W + 16, need, 0) == fa.FA_ERR_INVALID_ARG     # not 256-aligned
+    assert fa.fa_fwd_host_raw(*args, -1, W, need, 0) == fa.FA_ERR_INVALID_ARG         # negative chunk
+    assert fa.fa_fwd_host_raw(*PTRS, 1, 2, 256, 512, 48, 0.125, False, 0, W, need, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_host_raw(*PTRS, 0, 2, 256, 512, 64, 0.125, False, 0, W, need, 0) == fa.FA_OK  # empty

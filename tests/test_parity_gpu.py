@@ -217,6 +217,34 @@ def test_bf16_back_to_back_launches_on_two_streams():
         check_bf16(o0.float().cpu().numpy(), l0.cpu().numpy(), o_ref, lse_ref, f"problem {i}")
 
 
+@pytest.mark.parametrize("B,H,M,N,D,causal,chunk", [(2, 5, 300, 700, 128, True, 0), (1, 7, 1000, 513, 64, False, 3),
+                                                     (3, 2, 129, 0, 96, False, 4), (1, 1, 64, 200, 64, True, 1)])
+def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
+    """fa_fwd_host (host tensors, copies overlapped with the kernel through
+    two workspace slots) gives exactly fa_fwd's bits, for chunk sizes that
+    leave a ragged last chunk, and on a side stream."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    g = torch.Generator().manual_seed(B * 1000 + H * 10 + D)
+    q = torch.randn(B, H, M, D, generator=g).to(torch.bfloat16).pin_memory()
+    k = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16).pin_memory()
+    v = torch.randn(B, H, N, D, generator=g).to(torch.bfloat16).pin_memory()
+    o = torch.full((B, H, M, D), 7.0, dtype=torch.bfloat16).pin_memory()
+    lse = torch.zeros(B, H, M, dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream()
+    fa.fa_fwd_host(q, k, v, o, lse, D ** -0.5, causal, heads_per_chunk=chunk, stream=s)
+    s.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    do = torch.empty_like(dq)
+    dl = torch.empty(B, H, M, device="cuda")
+    fa.fa_fwd(dq, dk, dv, do, dl, D ** -0.5, causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o, do.cpu()) and torch.equal(lse, dl.cpu())
+
+
 # ------------------------------------------------ full-size workloads (sampled)
 
 def _full_size_check(w, heads, rows_per_head):
