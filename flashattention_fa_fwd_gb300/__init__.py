@@ -12,4 +12,4 @@ from ._binding import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_U
                        fa_fwd_host_workspace_bytes, fa_fwd_noalloc, fa_fwd_noalloc_raw,
                        fa_fwd_raw, fa_fwd_splitkv, fa_fwd_splitkv_raw, fa_fwd_splitkv_suggest,
                        fa_fwd_splitkv_workspace_bytes, fa_get_device_status,
-                       fa_last_error, fa_status_string, library_path, load_library)
+                       fa_last_error, fa_selftest_wait_timeout, fa_status_string, library_path, load_library)

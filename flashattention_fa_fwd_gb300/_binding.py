@@ -26,7 +26,7 @@ FA_ERR_TIMEOUT = 4
 
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
             "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest",
-            "fa_fwd_host", "fa_fwd_host_workspace_bytes")
+            "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_selftest_wait_timeout")
 
 
 class FaError(RuntimeError):
@@ -72,6 +72,8 @@ def load_library():
         lib.fa_fwd_host.restype = ctypes.c_int
         lib.fa_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
         lib.fa_fwd_host_workspace_bytes.restype = i64
+        lib.fa_selftest_wait_timeout.argtypes = [i64, vp]
+        lib.fa_selftest_wait_timeout.restype = ctypes.c_int
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = ctypes.c_int
         lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -129,6 +131,13 @@ def fa_fwd_host_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M:
 
 def fa_fwd_host_workspace_bytes(B: int, H: int, M: int, N: int, D: int, heads_per_chunk: int = 0) -> int:
     return load_library().fa_fwd_host_workspace_bytes(B, H, M, N, D, heads_per_chunk)
+
+
+def fa_selftest_wait_timeout(limit_us: int = 20000, stream: int = 0) -> int:
+    """Launches the bounded-wait self-test (a wait that nothing satisfies
+    gives up after ``limit_us``); returns the launch status. Read the outcome
+    with :func:`fa_get_device_status`, which should give FA_ERR_TIMEOUT."""
+    return load_library().fa_selftest_wait_timeout(int(limit_us), stream)
 
 
 def fa_status_string(status: int) -> str:

@@ -20,6 +20,7 @@
 
 #include "fa_fwd.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 #define FA_API extern "C" __attribute__((visibility("default")))
 
@@ -672,5 +673,41 @@ FA_API fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* 
     if (!check(cudaEventRecord(P->end, P->out), "cudaEventRecord") ||
         !check(cudaStreamWaitEvent(s, P->end, 0), "cudaStreamWaitEvent"))
         return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the failure path: a kernel waits, with the attention kernels'
+// bounded wait, on a barrier phase that nothing completes. The wait must give
+// up after `limit_ns`, OR FA timeout into the status word and return, leaving
+// the context usable; fa_get_device_status() then reports FA_ERR_TIMEOUT.
+// ---------------------------------------------------------------------------
+namespace {
+
+__global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        fa::mbar_init(fa::smem_u32(&bar), 1);
+        fa::fence_barrier_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`.
+    if (threadIdx.x == 0) (void)fa::mbar_wait(fa::smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+}
+
+}  // namespace
+
+FA_API fa_status fa_selftest_wait_timeout(int64_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(FA_ERR_INVALID_ARG, "limit_us must be in [1, 1000000] (got %lld)", (long long)limit_us);
+    uint32_t* word = nullptr;
+    fa_status st = device_setup(false, &word);
+    if (st != FA_OK) return st;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word,
+                                                                        static_cast<uint64_t>(limit_us) * 1000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launching the wait self-test");
     return FA_OK;
 }

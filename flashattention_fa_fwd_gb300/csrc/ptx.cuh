@@ -84,15 +84,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Waits for phase `parity` of barrier `bar`. Returns false, after setting
 // *abort (a CTA-wide shared flag) and the device error word, if the limit
-// passes; returns false at once if another role already set *abort.
+// (kWaitLimitNs unless given) passes; returns false at once if another role
+// already set *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* err_word) {
+                                          uint32_t* err_word, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             if (err_word) atomicOr(err_word, DEV_ERR_TIMEOUT);
             return false;

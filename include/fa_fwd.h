@@ -227,6 +227,20 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
                          int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
                          float scale, int causal, void* stream);
 
+/*
+ * Self-test of the library's failure detection (the pages have no
+ * counterpart: it checks this library's own bounded waits). Launches on
+ * `stream` one small kernel that waits, with the same bounded barrier wait
+ * the attention kernels use, on a barrier phase that nothing completes; after
+ * `limit_us` microseconds (1 .. 1000000) the wait gives up, records a timeout
+ * in the device status word and the kernel returns normally. A following
+ * fa_get_device_status() must return FA_ERR_TIMEOUT (and clear the word), and
+ * the CUDA context stays usable. Nothing faults, traps or hangs.
+ * Returns FA_ERR_INVALID_ARG for limit_us outside [1, 1000000], otherwise
+ * as fa_fwd's launch.
+ */
+fa_status fa_selftest_wait_timeout(int64_t limit_us, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(int status);
 

@@ -146,3 +146,8 @@ def test_host_entry_workspace_size_and_checks(lib):
     assert fa.fa_fwd_host_raw(*args, -1, W, need, 0) == fa.FA_ERR_INVALID_ARG         # negative chunk
     assert fa.fa_fwd_host_raw(*PTRS, 1, 2, 256, 512, 48, 0.125, False, 0, W, need, 0) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_host_raw(*PTRS, 0, 2, 256, 512, 64, 0.125, False, 0, W, need, 0) == fa.FA_OK  # empty
+
+
+def test_wait_selftest_rejects_bad_limits(lib):
+    assert fa.fa_selftest_wait_timeout(0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_selftest_wait_timeout(2_000_000) == fa.FA_ERR_INVALID_ARG

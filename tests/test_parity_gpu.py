@@ -245,6 +245,26 @@ def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
     assert torch.equal(o, do.cpu()) and torch.equal(lse, dl.cpu())
 
 
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a fault: a kernel waits, with the kernels'
+    bounded barrier wait, on a phase nothing completes. After 20 ms it gives
+    up and records a timeout; the status reads FA_ERR_TIMEOUT once, then OK,
+    and the next forward still matches the oracle."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    assert fa.fa_get_device_status() == fa.FA_OK
+    s = torch.cuda.current_stream().cuda_stream
+    assert fa.fa_selftest_wait_timeout(20000, s) == fa.FA_OK
+    assert fa.fa_get_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_get_device_status() == fa.FA_OK
+    q, k, v = (_rand((1, 2, 200, 64), 90 + i) for i in range(3))
+    o, lse = run_bf16(q, k, v, 0.125, True)
+    o_ref, lse_ref = attention(q, k, v, 0.125, True)
+    check_bf16(o, lse, o_ref, lse_ref, "after a timeout")
+
+
 # ------------------------------------------------ full-size workloads (sampled)
 
 def _full_size_check(w, heads, rows_per_head):
