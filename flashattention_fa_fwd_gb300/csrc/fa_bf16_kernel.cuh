@@ -8,8 +8,8 @@
 // key/value tiles stream past it; per row the kernel carries the running
 // max m, the running sum l and the unnormalised output acc, rescales l and
 // acc by alpha = exp2(m_old - m_new) when the max grows (see "Running max"
-// below), and divides by l once at the end. log2(e) is folded into the score scale so that each
-// score costs one FMA and one base-two exponential. The per-row log-sum-exp
+// below), and divides by l once at the end. log2(e) is folded into the score
+// scale so that each score costs one FMA and one base-two exponential. The per-row log-sum-exp
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
 // Work unit: one (batch*head, pair of 128-row query tiles). Each CTA is
@@ -54,7 +54,8 @@
 // Hand-offs (mbarriers): S_FULL (MMA -> softmax), P_FULL (softmax -> MMA),
 // per unit ST_FULL / ST_EMPTY (softmax <-> epilogue: m, l, l_o), O_DONE
 // (MMA -> epilogue), O_FREE (epilogue -> MMA: O_t may be overwritten by the
-// next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY (TMA ring).
+// next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY (TMA ring), UNIT_FULL /
+// UNIT_EMPTY (the ring of claimed unit indices).
 //
 // Causal (top-left, key j visible to query i when j <= i): key tiles wholly
 // above the diagonal are never loaded or multiplied; the diagonal tile and a
