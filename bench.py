@@ -437,6 +437,18 @@ def gpu_arm(args, w, rank, world, local_rank):
         return 0
 
     peak = float(peaks["bf16_tflops"])
+    bound, peak_source = "tensor", (f"{peaks.get('source')} bf16_tflops (burst); sustained "
+                                    f"{peaks.get('bf16_tflops_sustained')}")
+    frac_sust = achieved / float(peaks.get("bf16_tflops_sustained", peak))
+    if not bf16:
+        # The fp32 path runs on the CUDA cores (fp32 FMA, no tensor cores):
+        # its ceiling is SMs x 128 fp32 lanes x 2 FLOP per FMA x max SM clock.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        bound = "alu"
+        peak_source = f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x {mhz:.0f} MHz (fp32 FMA)"
+        frac_sust = None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, secs, nrows, cores, desc = oracle_sample(w, args.cpu_seconds)
@@ -451,12 +463,11 @@ def gpu_arm(args, w, rank, world, local_rank):
                        l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
                        if in_bytes > 129e6 else "inputs fit in L2 (warm)"),
         "pct_of_peak": 100.0 * value / world / peak,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 else None,
-                     "peak_source": f"{peaks.get('source')} bf16_tflops (burst); sustained "
-                                    f"{peaks.get('bf16_tflops_sustained')}",
-                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                     "peak_source": peak_source,
+                     "frac_of_sustained": frac_sust,
                      "launch_ms": launch_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
