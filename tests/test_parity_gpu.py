@@ -265,6 +265,62 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     check_bf16(o, lse, o_ref, lse_ref, "after a timeout")
 
 
+def test_bf16_random_shapes():
+    """Seeded random problems: any B, H, M, N (including 1 and values that
+    are not tile multiples), every supported D, causal or not, logit scales
+    from flat to peaked; each checked element by element against the oracle."""
+    rng = np.random.default_rng(20261202)
+    for case in range(24):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        M, N = int(rng.integers(1, 700)), int(rng.integers(1, 900))
+        D = int(rng.choice([64, 96, 128]))
+        causal = bool(rng.integers(0, 2))
+        sigma = float(rng.choice([0.5, 1.0, 2.5]))
+        seed = 1000 + case
+        q = _rand((B, H, M, D), seed, sigma)
+        k = _rand((B, H, N, D), seed + 1, sigma)
+        v = _rand((B, H, N, D), seed + 2)
+        scale = D ** -0.5
+        o, lse = run_bf16(q, k, v, scale, causal)
+        o_ref, lse_ref = attention(q, k, v, scale, causal)
+        check_bf16(o, lse, o_ref, lse_ref, f"case {case}: B{B} H{H} M{M} N{N} D{D} causal={causal} sigma={sigma}")
+
+
+def test_bf16_cuda_graph_replays():
+    """fa_fwd captured once in a CUDA graph and replayed: every replay starts
+    the work-unit counter from zero (the last CTA of each launch resets it)
+    and gives the same bits as a direct call, for new inputs copied in."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    B, H, M, N, D = 2, 3, 700, 900, 128
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q = torch.randn(B, H, M, D, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, N, D, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, N, D, device="cuda", generator=g).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, M, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fa_fwd(q, k, v, o, lse, D ** -0.5, True)   # first call on the device outside the capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fa.fa_fwd(q, k, v, o, lse, D ** -0.5, True)
+    for rep in range(5):
+        with torch.no_grad():
+            q.copy_(torch.randn(B, H, M, D, device="cuda", generator=g).to(torch.bfloat16))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        o2, l2 = torch.empty_like(o), torch.empty_like(lse)
+        fa.fa_fwd(q, k, v, o2, l2, D ** -0.5, True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o2) and torch.equal(lse, l2), f"replay {rep}"
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
 # ------------------------------------------------ full-size workloads (sampled)
 
 def _full_size_check(w, heads, rows_per_head):
