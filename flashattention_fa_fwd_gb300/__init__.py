@@ -8,7 +8,8 @@ the library; the first call does, and raises if it has not been built.
 """
 
 from ._binding import (FA_ERR_CUDA, FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK,  # noqa: F401
-                       FaError, fa_fwd, fa_fwd_f32, fa_fwd_f32_raw, fa_fwd_host, fa_fwd_host_raw,
+                       FaError, fa_bwd, fa_bwd_raw, fa_bwd_workspace_bytes, fa_fwd, fa_fwd_f32, fa_fwd_f32_raw,
+                       fa_fwd_host, fa_fwd_host_raw,
                        fa_fwd_host_workspace_bytes, fa_fwd_noalloc, fa_fwd_noalloc_raw,
                        fa_fwd_raw, fa_fwd_splitkv, fa_fwd_splitkv_raw, fa_fwd_splitkv_suggest,
                        fa_fwd_splitkv_workspace_bytes, fa_get_device_status,

@@ -26,7 +26,8 @@ FA_ERR_TIMEOUT = 4
 
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
             "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest",
-            "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_selftest_wait_timeout")
+            "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_selftest_wait_timeout", "fa_bwd",
+            "fa_bwd_workspace_bytes")
 
 
 class FaError(RuntimeError):
@@ -72,6 +73,10 @@ def load_library():
         lib.fa_fwd_host.restype = ctypes.c_int
         lib.fa_fwd_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
         lib.fa_fwd_host_workspace_bytes.restype = i64
+        lib.fa_bwd.argtypes = [vp] * 9 + [i64] * 5 + [ctypes.c_float, ctypes.c_int, vp, i64, vp]
+        lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.fa_bwd_workspace_bytes.restype = i64
         lib.fa_selftest_wait_timeout.argtypes = [i64, vp]
         lib.fa_selftest_wait_timeout.restype = ctypes.c_int
         lib.fa_get_device_status.argtypes = [vp]
@@ -138,6 +143,18 @@ def fa_selftest_wait_timeout(limit_us: int = 20000, stream: int = 0) -> int:
     gives up after ``limit_us``); returns the launch status. Read the outcome
     with :func:`fa_get_device_status`, which should give FA_ERR_TIMEOUT."""
     return load_library().fa_selftest_wait_timeout(int(limit_us), stream)
+
+
+def fa_bwd_raw(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int, dv: int, B: int, H: int,
+               M: int, N: int, D: int, scale: float, causal: bool, workspace: int, workspace_bytes: int,
+               stream: int = 0) -> int:
+    """Calls fa_bwd with raw device addresses; returns the status."""
+    return load_library().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, M, N, D, float(scale),
+                                 int(bool(causal)), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, M: int) -> int:
+    return load_library().fa_bwd_workspace_bytes(B, H, M)
 
 
 def fa_status_string(status: int) -> str:
@@ -312,3 +329,29 @@ def fa_fwd_host(q, k, v, o, lse, scale: float, causal: bool = False, heads_per_c
                              workspace.numel(), s)
     if st != FA_OK:
         raise FaError(st, "fa_fwd_host")
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool = False, workspace=None,
+           stream=None) -> None:
+    """Gradients of :func:`fa_fwd`: writes fp32 ``dq``, ``dk``, ``dv`` from the
+    bf16 inputs ``q``, ``k``, ``v``, the forward's ``o`` (bf16) and ``lse``
+    (fp32), and the bf16 output gradient ``dout``. ``workspace`` is a CUDA
+    tensor of at least fa_bwd_workspace_bytes(B, H, M) bytes (allocated here
+    when None)."""
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.bfloat16)
+    if dout.dtype != torch.bfloat16 or not dout.is_cuda or not dout.is_contiguous() or _shape4(dout, "dout") != (B, H, M, D):
+        raise ValueError("dout must be a contiguous bf16 CUDA tensor shaped like q")
+    for name, t, rows in (("dq", dq, M), ("dk", dk, N), ("dv", dv, N)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or _shape4(t, name) != (B, H, rows, D):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape [B, H, {rows}, D]")
+    with torch.cuda.device(q.device):
+        need = fa_bwd_workspace_bytes(B, H, M)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, M, N, D, scale, causal,
+                        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")

@@ -711,3 +711,67 @@ FA_API fa_status fa_selftest_wait_timeout(int64_t limit_us, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "launching the wait self-test");
     return FA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// fa_bwd: gradients of the bf16 forward (see fa_bwd.cu).
+// ---------------------------------------------------------------------------
+FA_API int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t M) {
+    if (B < 0 || H < 0 || M < 0) return -1;
+    return B * H * M * static_cast<int64_t>(sizeof(float));
+}
+
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, float* dq, float* dk, float* dv, int64_t B, int64_t H, int64_t M,
+                        int64_t N, int64_t D, float scale, int causal, void* workspace, int64_t workspace_bytes,
+                        void* stream) {
+    bool empty = false;
+    // q, k, v and the forward's o / lse pass the forward's checks.
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 2, &empty);
+    if (st != FA_OK) return st;
+    if (D > 128) return fail(FA_ERR_UNSUPPORTED, "fa_bwd supports D <= 128 (got %lld)", (long long)D);
+    const int64_t bh = B * H;
+    const int64_t need = fa_bwd_workspace_bytes(B, H, M);
+    if (bh == 0 || (M == 0 && N == 0)) return FA_OK;
+    if ((M > 0 && (dout == nullptr || dq == nullptr)) || (N > 0 && (dk == nullptr || dv == nullptr)))
+        return fail(FA_ERR_INVALID_ARG, "dout, dq, dk and dv must not be null for non-empty tensors");
+    if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+        return fail(FA_ERR_INVALID_ARG, "dout, dq, dk and dv must be 16-byte aligned");
+    if (M > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(FA_ERR_INVALID_ARG, "workspace of %lld bytes needed (got %lld)", (long long)need,
+                    (long long)workspace_bytes);
+    if (M > 0 && !aligned(workspace, 16)) return fail(FA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const int64_t qb = bh * M * D * 4, kb = bh * N * D * 4;
+    if (overlaps(dq, qb, dk, kb) || overlaps(dq, qb, dv, kb) || overlaps(dk, kb, dv, kb) ||
+        overlaps(dq, qb, q, bh * M * D * 2) || overlaps(dk, kb, k, bh * N * D * 2) || overlaps(dv, kb, v, bh * N * D * 2) ||
+        overlaps(workspace, need, dq, qb) || overlaps(workspace, need, dk, kb) || overlaps(workspace, need, dv, kb))
+        return fail(FA_ERR_INVALID_ARG, "the gradients and the workspace must not overlap each other or the inputs");
+    uint32_t* word = nullptr;
+    if ((st = device_setup(false, &word)) != FA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (M == 0) {   // no query rows: every key gets zero gradient
+        e = cudaMemsetAsync(dk, 0, kb, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kb, s);
+        return e == cudaSuccess ? FA_OK : cuda_fail(e, "clearing dk and dv");
+    }
+    fa::BwdParams p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.o = static_cast<const __nv_bfloat16*>(o);
+    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.lse = lse;
+    p.delta = static_cast<float*>(workspace);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.bh_count = static_cast<int>(bh);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.scale = scale;
+    p.causal = causal != 0;
+    e = fa::launch_bwd(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the backward kernels");
+    return FA_OK;
+}

@@ -1,0 +1,222 @@
+// Backward pass of the attention forward, on the CUDA cores (fp32 arithmetic).
+//
+// "Module 08: FlashAttention and Memory-Efficient Kernels", section "The
+// backward pass: recompute instead of store" and Code Step 6: the forward
+// keeps one number per row, L = m + log(l), and the backward rebuilds every
+// tile of P on chip as exp(S - L) from Q and K instead of reading a stored
+// N x N matrix. With that P, for an output gradient dO:
+//   dV = P^T dO,  dP = dO V^T,  Dl_i = sum_d dO_id O_id,
+//   dS = P * (dP - Dl),  dQ = scale dS K,  dK = scale dS^T Q.
+// Three kernels, each reading bf16 inputs and accumulating in fp32:
+//   bwd_rowdot: Dl_i for every query row (one warp per row);
+//   bwd_dkdv:   one CTA per 64-key tile of one head; query rows stream through
+//               shared memory in chunks; dK and dV of the tile stay in
+//               registers (four threads per key, each holding a quarter of D);
+//   bwd_dq:     one CTA per 64-row query tile; key rows stream through shared
+//               memory; dQ stays in registers.
+// The two main kernels both rebuild P (and dP) -- seven products' worth of
+// work against the five of Practice 3 -- so that no output needs atomics and
+// the result is deterministic. The scores use exp2 with log2(e) folded into
+// the scale, as the forward does.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+namespace {
+
+constexpr int kTile = 64;      // keys (dK/dV kernel) or query rows (dQ kernel) per CTA
+constexpr int kParts = 4;      // threads sharing one key or row, each over DV/4 of D
+constexpr int kThreads = kTile * kParts;
+constexpr int kChunk = 32;     // rows streamed through shared memory per step
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// Sum over the kParts consecutive lanes that share a key or row.
+__device__ __forceinline__ float part_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    return x;
+}
+
+__global__ void bwd_rowdot(const BwdParams p) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= static_cast<int64_t>(p.bh_count) * p.M) return;
+    const __nv_bfloat16* o = p.o + row * p.D;
+    const __nv_bfloat16* d = p.dout + row * p.D;
+    float s = 0.f;
+    for (int i = lane; i < p.D; i += 32) s = fmaf(ld_bf16(o + i), ld_bf16(d + i), s);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) p.delta[row] = s;
+}
+
+// Copies `rows` rows of width D (bf16, row-major) starting at row r0 into
+// shared memory as fp32 [kChunk][DV], zero-filling rows >= limit and
+// columns >= D.
+template <int DV>
+__device__ __forceinline__ void stage(float* dst, const __nv_bfloat16* src, int r0, int limit, int D) {
+    for (int i = threadIdx.x; i < kChunk * DV; i += kThreads) {
+        const int r = i / DV, c = i % DV;
+        dst[i] = (r0 + r < limit && c < D) ? ld_bf16(src + static_cast<int64_t>(r0 + r) * D + c) : 0.f;
+    }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
+    constexpr int W = DV / kParts;
+    __shared__ float sq[kChunk * DV], sdo[kChunk * DV], slse[kChunk], sdl[kChunk];
+    const int tiles = (p.N + kTile - 1) / kTile;
+    const int bh = blockIdx.x / tiles;
+    const int key0 = (blockIdx.x - bh * tiles) * kTile;
+    const int key = key0 + threadIdx.x / kParts;
+    const int c0 = (threadIdx.x % kParts) * W;            // this thread's columns [c0, c0 + W)
+    const bool kvalid = key < p.N;
+    const int64_t kv_base = static_cast<int64_t>(bh) * p.N * p.D;
+    const int64_t q_base = static_cast<int64_t>(bh) * p.M * p.D;
+    float kr[W], vr[W], dk[W], dv[W];
+#pragma unroll
+    for (int c = 0; c < W; ++c) {
+        const bool in = kvalid && c0 + c < p.D;
+        kr[c] = in ? ld_bf16(p.k + kv_base + static_cast<int64_t>(key) * p.D + c0 + c) : 0.f;
+        vr[c] = in ? ld_bf16(p.v + kv_base + static_cast<int64_t>(key) * p.D + c0 + c) : 0.f;
+        dk[c] = 0.f;
+        dv[c] = 0.f;
+    }
+    const float cs = p.scale * kLog2e;
+    // Query rows that can see a key of this tile: all, or (causal) rows >= key0.
+    const int row_lo = p.causal ? key0 : 0;
+    for (int r0 = row_lo; r0 < p.M; r0 += kChunk) {
+        __syncthreads();
+        stage<DV>(sq, p.q + q_base, r0, p.M, p.D);
+        stage<DV>(sdo, p.dout + q_base, r0, p.M, p.D);
+        for (int i = threadIdx.x; i < kChunk; i += kThreads) {
+            const bool in = r0 + i < p.M;
+            const int64_t row = static_cast<int64_t>(bh) * p.M + r0 + i;
+            slse[i] = in ? p.lse[row] : -INFINITY;
+            sdl[i] = in ? p.delta[row] : 0.f;
+        }
+        __syncthreads();
+        for (int i = 0; i < kChunk; ++i) {
+            const int row = r0 + i;
+            const float* qi = sq + i * DV + c0;
+            const float* doi = sdo + i * DV + c0;
+            float s = 0.f, dp = 0.f;
+#pragma unroll
+            for (int c = 0; c < W; ++c) {
+                s = fmaf(kr[c], qi[c], s);
+                dp = fmaf(vr[c], doi[c], dp);
+            }
+            s = part_sum(s);
+            dp = part_sum(dp);
+            const bool vis = kvalid && row < p.M && (!p.causal || key <= row) && slse[i] != -INFINITY;
+            const float pr = vis ? exp2f(fmaf(s, cs, -slse[i] * kLog2e)) : 0.f;
+            const float ds = pr * (dp - sdl[i]);
+#pragma unroll
+            for (int c = 0; c < W; ++c) {
+                dv[c] = fmaf(pr, doi[c], dv[c]);
+                dk[c] = fmaf(ds, qi[c], dk[c]);
+            }
+        }
+    }
+    if (!kvalid) return;
+    const int64_t out = kv_base + static_cast<int64_t>(key) * p.D;
+#pragma unroll
+    for (int c = 0; c < W; ++c) {
+        if (c0 + c < p.D) {
+            p.dk[out + c0 + c] = dk[c] * p.scale;
+            p.dv[out + c0 + c] = dv[c];
+        }
+    }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(kThreads) bwd_dq(const BwdParams p) {
+    constexpr int W = DV / kParts;
+    __shared__ float sk[kChunk * DV], sv[kChunk * DV];
+    const int tiles = (p.M + kTile - 1) / kTile;
+    const int bh = blockIdx.x / tiles;
+    const int row0 = (blockIdx.x - bh * tiles) * kTile;
+    const int row = row0 + threadIdx.x / kParts;
+    const int c0 = (threadIdx.x % kParts) * W;
+    const bool rvalid = row < p.M;
+    const int64_t q_base = static_cast<int64_t>(bh) * p.M * p.D;
+    const int64_t kv_base = static_cast<int64_t>(bh) * p.N * p.D;
+    float qr[W], dor[W], dq[W];
+#pragma unroll
+    for (int c = 0; c < W; ++c) {
+        const bool in = rvalid && c0 + c < p.D;
+        qr[c] = in ? ld_bf16(p.q + q_base + static_cast<int64_t>(row) * p.D + c0 + c) : 0.f;
+        dor[c] = in ? ld_bf16(p.dout + q_base + static_cast<int64_t>(row) * p.D + c0 + c) : 0.f;
+        dq[c] = 0.f;
+    }
+    const float lse = rvalid ? p.lse[static_cast<int64_t>(bh) * p.M + row] : -INFINITY;
+    const float dl = rvalid ? p.delta[static_cast<int64_t>(bh) * p.M + row] : 0.f;
+    const float cs = p.scale * kLog2e;
+    // Keys any row of this tile can see: all, or (causal) keys <= its last row.
+    const int key_hi = p.causal ? min(p.N, min(p.M, row0 + kTile)) : p.N;
+    for (int k0 = 0; k0 < key_hi; k0 += kChunk) {
+        __syncthreads();
+        stage<DV>(sk, p.k + kv_base, k0, p.N, p.D);
+        stage<DV>(sv, p.v + kv_base, k0, p.N, p.D);
+        __syncthreads();
+        for (int j = 0; j < kChunk; ++j) {
+            const int key = k0 + j;
+            const float* kj = sk + j * DV + c0;
+            const float* vj = sv + j * DV + c0;
+            float s = 0.f, dp = 0.f;
+#pragma unroll
+            for (int c = 0; c < W; ++c) {
+                s = fmaf(qr[c], kj[c], s);
+                dp = fmaf(dor[c], vj[c], dp);
+            }
+            s = part_sum(s);
+            dp = part_sum(dp);
+            const bool vis = rvalid && key < p.N && (!p.causal || key <= row) && lse != -INFINITY;
+            const float pr = vis ? exp2f(fmaf(s, cs, -lse * kLog2e)) : 0.f;
+            const float ds = pr * (dp - dl);
+#pragma unroll
+            for (int c = 0; c < W; ++c) dq[c] = fmaf(ds, kj[c], dq[c]);
+        }
+    }
+    if (!rvalid) return;
+    const int64_t out = q_base + static_cast<int64_t>(row) * p.D;
+#pragma unroll
+    for (int c = 0; c < W; ++c)
+        if (c0 + c < p.D) p.dq[out + c0 + c] = dq[c] * p.scale;
+}
+
+template <int DV>
+cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
+    const int64_t kv_blocks = static_cast<int64_t>(p.bh_count) * ((p.N + kTile - 1) / kTile);
+    const int64_t q_blocks = static_cast<int64_t>(p.bh_count) * ((p.M + kTile - 1) / kTile);
+    if (kv_blocks > 0x7fffffffLL || q_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (kv_blocks > 0) bwd_dkdv<DV><<<static_cast<unsigned>(kv_blocks), kThreads, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq<DV><<<static_cast<unsigned>(q_blocks), kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(p.bh_count) * p.M;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    bwd_rowdot<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.D <= 32) return launch_bwd_t<32>(p, s);
+    if (p.D <= 64) return launch_bwd_t<64>(p, s);
+    return launch_bwd_t<128>(p, s);
+}
+
+}  // namespace fa

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace fa {
@@ -56,6 +57,30 @@ struct F32Params {
 };
 
 cudaError_t launch_f32(const F32Params& p, bool causal, cudaStream_t s);
+
+// Arguments of the backward kernels: bf16 inputs of the forward plus its O,
+// LSE and the output gradient dO; fp32 gradients out.
+struct BwdParams {
+    const __nv_bfloat16* q;      // [BH, M, D]
+    const __nv_bfloat16* k;      // [BH, N, D]
+    const __nv_bfloat16* v;      // [BH, N, D]
+    const __nv_bfloat16* o;      // [BH, M, D] forward output
+    const __nv_bfloat16* dout;   // [BH, M, D] gradient of the loss with respect to O
+    const float* lse;            // [BH, M] forward log-sum-exp (natural log)
+    float* delta;                // [BH, M] workspace: sum_d dO * O per row
+    float* dq;                   // [BH, M, D]
+    float* dk;                   // [BH, N, D]
+    float* dv;                   // [BH, N, D]
+    int bh_count;
+    int M;
+    int N;
+    int D;
+    float scale;
+    int causal;
+};
+
+// Launches the three backward kernels (row dots, dK/dV, dQ) on `s`.
+cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s);
 
 // Merges split-KV partial results: for every row, LSE = ln sum_s exp(LSE_s)
 // and O = sum_s exp(LSE_s - LSE) O_s, written as bf16 O and fp32 LSE.

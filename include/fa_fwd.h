@@ -228,6 +228,41 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
                          float scale, int causal, void* stream);
 
 /*
+ * Backward pass of fa_fwd: the gradients dQ, dK, dV of a loss whose gradient
+ * with respect to O is `dout`. "Module 08: FlashAttention and
+ * Memory-Efficient Kernels", section "The backward pass: recompute instead of
+ * store" and Code Step 6: nothing N x N is stored by the forward; every tile
+ * of P is rebuilt as exp(S - L) from Q, K and the forward's per-row
+ * log-sum-exp L (`lse`). With that P: dV = P^T dO, dP = dO V^T,
+ * dS = P * (dP - rowsum(dO * O)), dQ = scale dS K, dK = scale dS^T Q.
+ * This first version runs on the CUDA cores with fp32 arithmetic (bf16
+ * inputs read exactly) and is deterministic (no atomics).
+ *
+ *   q, k, v          the forward's bf16 inputs, [B,H,M,D] / [B,H,N,D]
+ *   o, lse           the forward's outputs for them (bf16 O, fp32 LSE)
+ *   dout             bf16 [B,H,M,D]
+ *   dq               fp32 [B,H,M,D], written
+ *   dk, dv           fp32 [B,H,N,D], written (rows no query sees get 0)
+ *   workspace        device memory owned by the caller, 16-byte aligned,
+ *                    at least fa_bwd_workspace_bytes(B, H, M) bytes
+ *   D                1..128
+ *
+ * Asynchronous on `stream`, never synchronises. Errors: the forward's
+ * checks on q, k, v, o, lse and the sizes, plus FA_ERR_INVALID_ARG for a
+ * null or misaligned dout / dq / dk / dv, a missing or short workspace, or
+ * gradients that overlap each other, the inputs or the workspace, and
+ * FA_ERR_UNSUPPORTED for D > 128.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, float* dq, float* dk, float* dv,
+                 int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                 float scale, int causal, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_bwd needs: B*H*M fp32 values (-1 for negative sizes).
+ * Needs no GPU. */
+int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t M);
+
+/*
  * Self-test of the library's failure detection (the pages have no
  * counterpart: it checks this library's own bounded waits). Launches on
  * `stream` one small kernel that waits, with the same bounded barrier wait

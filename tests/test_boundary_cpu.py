@@ -151,3 +151,23 @@ def test_host_entry_workspace_size_and_checks(lib):
 def test_wait_selftest_rejects_bad_limits(lib):
     assert fa.fa_selftest_wait_timeout(0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_selftest_wait_timeout(2_000_000) == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_size_and_checks(lib):
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 4
+    assert fa.fa_bwd_workspace_bytes(-1, 3, 100) == -1
+    W = 64 * A
+    grads = (6 * A, 7 * A, 8 * A)
+    args = (*PTRS, 9 * A, *grads, 1, 2, 256, 512, 64, 0.125, False)
+    need = fa.fa_bwd_workspace_bytes(1, 2, 256)
+    assert fa.fa_bwd_raw(*args, 0, need, 0) == fa.FA_ERR_INVALID_ARG             # missing workspace
+    assert fa.fa_bwd_raw(*args, W, need - 4, 0) == fa.FA_ERR_INVALID_ARG         # short workspace
+    assert fa.fa_bwd_raw(*PTRS, 9 * A, 0, 7 * A, 8 * A, 1, 2, 256, 512, 64, 0.125, False, W, need, 0) \
+        == fa.FA_ERR_INVALID_ARG                                                  # null dq
+    assert fa.fa_bwd_raw(*PTRS, 9 * A, 6 * A + 4, 7 * A, 8 * A, 1, 2, 256, 512, 64, 0.125, False, W, need, 0) \
+        == fa.FA_ERR_INVALID_ARG                                                  # misaligned dq
+    assert fa.fa_bwd_raw(*PTRS, 9 * A, *grads, 1, 2, 256, 512, 192, 0.125, False, W, need, 0) \
+        == fa.FA_ERR_UNSUPPORTED                                                  # D > 128
+    assert fa.fa_bwd_raw(*PTRS, 9 * A, 6 * A, 6 * A, 8 * A, 1, 2, 256, 512, 64, 0.125, False, W, need, 0) \
+        == fa.FA_ERR_INVALID_ARG                                                  # dq overlaps dk
+    assert fa.fa_bwd_raw(*PTRS, 9 * A, *grads, 0, 2, 256, 512, 64, 0.125, False, 0, 0, 0) == fa.FA_OK  # empty

@@ -12,7 +12,7 @@ import math
 import numpy as np
 import pytest
 
-from oracle import attention, attention_rows
+from oracle import attention, attention_bwd, attention_rows
 from flashattention_fa_fwd_gb300.inputs import WORKLOADS, head_tensor, make_inputs, round_to_bf16, sample_rows
 from parity import check_bf16, check_f32, run_bf16, run_f32
 
@@ -319,6 +319,63 @@ def test_bf16_cuda_graph_replays():
         torch.cuda.synchronize()
         assert torch.equal(o, o2) and torch.equal(lse, l2), f"replay {rep}"
     assert fa.fa_get_device_status() == fa.FA_OK
+
+
+# ------------------------------------------------------------ backward pass
+#
+# Tolerance: the backward reads the forward's bf16 O, whose rounding (half a
+# bf16 unit, 2^-9 relative) enters Dl = rowsum(dO * O) and through it every
+# element of dS; the kernels themselves add only fp32 rounding. Each gradient
+# must match the fp64 oracle (run on the same bf16 inputs) within
+# 1e-2 * max|reference| + 1e-4 element by element: five times the O-rounding
+# bound.
+BWD_RTOL_OF_MAX = 1e-2
+
+
+def _check_grad(g, ref, what):
+    g = np.asarray(g, dtype=np.float64)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite"
+    bound = BWD_RTOL_OF_MAX * float(np.abs(ref).max(initial=0.0)) + 1e-4
+    err = np.abs(g - ref)
+    assert err.max(initial=0.0) <= bound, f"{what}: max err {err.max():.3e} > {bound:.3e}"
+    return float(err.max(initial=0.0))
+
+
+@pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 200, 300, 64, False), (2, 1, 257, 129, 128, True),
+                                              (1, 3, 100, 100, 96, True), (1, 1, 1, 7, 64, False),
+                                              (1, 2, 190, 70, 32, True), (1, 1, 64, 64, 17, False)])
+def test_bwd_matches_oracle(B, H, M, N, D, causal):
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from parity import to_device_bf16
+
+    seed = B * 1000 + H * 100 + M + N + D
+    q, k, v = _rand((B, H, M, D), seed), _rand((B, H, N, D), seed + 1), _rand((B, H, N, D), seed + 2)
+    do = _rand((B, H, M, D), seed + 3)
+    scale = D ** -0.5
+    tq, tk, tv, tdo = (to_device_bf16(x) for x in (q, k, v, do))
+    if D in (64, 96, 128):
+        o = torch.empty_like(tq)
+        lse = torch.empty(B, H, M, device="cuda")
+        fa.fa_fwd(tq, tk, tv, o, lse, scale, causal)
+    else:   # no bf16 forward kernel for this D: the oracle's O (rounded to bf16) and LSE
+        o_np, lse_np = attention(q, k, v, scale, causal)
+        o, lse = to_device_bf16(o_np), torch.from_numpy(lse_np.astype(np.float32)).cuda()
+    grads = []
+    for _ in range(2):
+        dq = torch.empty(B, H, M, D, device="cuda")
+        dk = torch.empty(B, H, N, D, device="cuda")
+        dv = torch.empty(B, H, N, D, device="cuda")
+        fa.fa_bwd(tq, tk, tv, o, lse, tdo, dq, dk, dv, scale, causal)
+        torch.cuda.synchronize()
+        grads.append((dq, dk, dv))
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for a, b in zip(grads[0], grads[1]):
+        assert torch.equal(a, b), "backward is not deterministic"
+    ref = attention_bwd(q, k, v, do, scale, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), grads[0], ref):
+        _check_grad(g.cpu().numpy(), r, f"{name} B{B} H{H} M{M} N{N} D{D} causal={causal}")
 
 
 # ------------------------------------------------ full-size workloads (sampled)
