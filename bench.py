@@ -44,6 +44,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fwd attention TFLOP/s (4·B·H·M·N·D, causal ×½), % of BF16 tensor-core peak"
+METRIC_BWD = "bwd attention TFLOP/s (10·B·H·M·N·D: five M·N·D products, causal ×½)"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "causal_b8_h32_s4096_d128"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
@@ -64,6 +65,8 @@ def parse_args(argv=None):
                     help="time fa_fwd_splitkv with S key-range splits (0 = the library's suggestion)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward pass fa_bwd on the workload")
     return ap.parse_args(argv)
 
 
@@ -342,6 +345,23 @@ def gpu_arm(args, w, rank, world, local_rank):
     def step():
         call(q, k, v, o, lse, w.scale, w.causal)
 
+    bwd = args.pass_ == "bwd"
+    flops = w.flops
+    if bwd:
+        if not bf16 or splits > 1:
+            raise SystemExit("--pass bwd times fa_bwd: a bf16 workload, without --splitkv")
+        call(q, k, v, o, lse, w.scale, w.causal)        # the forward whose O and LSE the backward reads
+        gen = torch.Generator(device=dev).manual_seed(7)
+        dout = torch.randn(q.shape, device=dev, generator=gen).to(torch.bfloat16)
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        ws_bwd = torch.empty(max(fa.fa_bwd_workspace_bytes(w.B, w.H, w.M), 16), dtype=torch.uint8, device=dev)
+        flops = w.flops * 2.5    # five products instead of the forward's two
+
+        def step():
+            fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, w.scale, w.causal, workspace=ws_bwd)
+
     for _ in range(max(args.warmup, 3)):
         step()
     st = fa.fa_get_device_status()
@@ -384,9 +404,9 @@ def gpu_arm(args, w, rank, world, local_rank):
     if st != fa.FA_OK:
         raise SystemExit(f"device status after the timed region: {fa.fa_status_string(st)}")
     max_ms = max_over_ranks(elapsed_ms, world, dev)
-    value = whole_job_value(w.flops, steps, world, max_ms)
+    value = whole_job_value(flops, steps, world, max_ms)
     launch_ms = statistics.mean(per_launch)
-    achieved = w.flops / (launch_ms * 1e-3) / 1e12
+    achieved = flops / (launch_ms * 1e-3) / 1e12
 
     # End to end through the public call with host buffers.
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -395,7 +415,21 @@ def gpu_arm(args, w, rank, world, local_rank):
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
     e2e_api = "host copies + device call"
-    if bf16 and splits == 1:
+    if bwd:
+        hdo = dout.cpu().pin_memory()
+        ho.copy_(o)
+        hl.copy_(lse)
+        hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ho, hl, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (o, ho), (lse, hl), (dout, hdo)):
+                dst.copy_(src, non_blocking=True)
+            fa.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, w.scale, w.causal, workspace=ws_bwd)
+            for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+    elif bf16 and splits == 1:
         e2e_api = "fa_fwd_host (copies overlapped with the kernel, default chunks)"
         ws_host = torch.empty(max(fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.M, w.N, w.D, 0), 256),
                               dtype=torch.uint8, device=dev)
@@ -426,7 +460,7 @@ def gpu_arm(args, w, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), world, dev)
-    e2e_value = whole_job_value(w.flops, args.e2e_steps, world, e2e_ms)
+    e2e_value = whole_job_value(flops, args.e2e_steps, world, e2e_ms)
     assert bool(torch.isfinite(hl).all()), "non-finite LSE in the end-to-end result"
 
     if world > 1:
@@ -440,8 +474,8 @@ def gpu_arm(args, w, rank, world, local_rank):
     bound, peak_source = "tensor", (f"{peaks.get('source')} bf16_tflops (burst); sustained "
                                     f"{peaks.get('bf16_tflops_sustained')}")
     frac_sust = achieved / float(peaks.get("bf16_tflops_sustained", peak))
-    if not bf16:
-        # The fp32 path runs on the CUDA cores (fp32 FMA, no tensor cores):
+    if not bf16 or bwd:
+        # The fp32 path and the backward run on the CUDA cores (fp32 FMA, no tensor cores):
         # its ceiling is SMs x 128 fp32 lanes x 2 FLOP per FMA x max SM clock.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         mhz = float(peaks.get("sm_max_mhz", 2070.0))
@@ -456,7 +490,7 @@ def gpu_arm(args, w, rank, world, local_rank):
                "seconds": secs}
     in_bytes = h2d
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": max_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas x{world}", kv_splits=splits,
@@ -465,14 +499,14 @@ def gpu_arm(args, w, rank, world, local_rank):
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 else None,
+                     "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 and not bwd else None,
                      "peak_source": peak_source,
                      "frac_of_sustained": frac_sust,
                      "launch_ms": launch_ms},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps, "api": e2e_api},
-        "gpu_launches": steps * (2 if splits > 1 else 1),
+        "gpu_launches": steps * (3 if bwd else (2 if splits > 1 else 1)),
         "clocks": clocks,
         "clocks_rejected": clocks_rejected(clocks),
     }
