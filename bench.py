@@ -65,6 +65,8 @@ def parse_args(argv=None):
                     help="time fa_fwd_splitkv with S key-range splits (0 = the library's suggestion)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
+    ap.add_argument("--f32-path", choices=["ieee", "x3"], default="ieee",
+                    help="fp32 workloads: exact CUDA-core fa_fwd_f32 (ieee) or tensor-core fa_fwd_f32x3 (x3)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward pass fa_bwd on the workload")
     return ap.parse_args(argv)
@@ -340,6 +342,13 @@ def gpu_arm(args, w, rank, world, local_rank):
 
         def call(q_, k_, v_, o_, l_, scale_, causal_):
             fa.fa_fwd_splitkv(q_, k_, v_, o_, l_, scale_, causal_, num_splits=splits, workspace=ws)
+    x3 = not bf16 and args.f32_path == "x3"
+    if x3:
+        ws_x3 = torch.empty(max(fa.fa_fwd_f32x3_workspace_bytes(w.B, w.H, w.N, w.D), 16), dtype=torch.uint8,
+                            device=dev)
+
+        def call(q_, k_, v_, o_, l_, scale_, causal_):
+            fa.fa_fwd_f32x3(q_, k_, v_, o_, l_, scale_, causal_, workspace=ws_x3)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -474,7 +483,15 @@ def gpu_arm(args, w, rank, world, local_rank):
     bound, peak_source = "tensor", (f"{peaks.get('source')} bf16_tflops (burst); sustained "
                                     f"{peaks.get('bf16_tflops_sustained')}")
     frac_sust = achieved / float(peaks.get("bf16_tflops_sustained", peak))
-    if not bf16 or bwd:
+    if x3:
+        # Three TF32 products per matrix product: the tensor core executes 3x the attention
+        # FLOPs, against the TF32 peak (measured bf16 x the nominal TF32 : BF16 ratio 1.1 : 2.25).
+        achieved *= 3.0
+        peak = float(peaks["bf16_tflops"]) * 1.1 / 2.25
+        peak_source = (f"{peaks.get('source')} bf16_tflops x 1.1/2.25 (nominal dense TF32 : BF16); achieved "
+                       f"counts the 3 TF32 products per attention FLOP")
+        frac_sust = achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * 1.1 / 2.25)
+    elif not bf16 or bwd:
         # The fp32 path and the backward run on the CUDA cores (fp32 FMA, no tensor cores):
         # its ceiling is SMs x 128 fp32 lanes x 2 FLOP per FMA x max SM clock.
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -494,9 +511,10 @@ def gpu_arm(args, w, rank, world, local_rank):
         "warmup": max(args.warmup, 3), "ms_per_step": max_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas x{world}", kv_splits=splits,
+                       **({"f32_path": "x3 (fa_fwd_f32x3)" if x3 else "ieee (fa_fwd_f32)"} if not bf16 else {}),
                        l2=f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
                        if in_bytes > 129e6 else "inputs fit in L2 (warm)"),
-        "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_peak": 100.0 * value / world * (3.0 if x3 else 1.0) / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 and not bwd else None,
@@ -506,7 +524,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps, "api": e2e_api},
-        "gpu_launches": steps * (3 if bwd else (2 if splits > 1 else 1)),
+        "gpu_launches": steps * (3 if bwd else (2 if splits > 1 or x3 else 1)),
         "clocks": clocks,
         "clocks_rejected": clocks_rejected(clocks),
     }

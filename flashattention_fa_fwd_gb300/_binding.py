@@ -27,7 +27,7 @@ FA_ERR_TIMEOUT = 4
 EXPORTED = ("fa_fwd", "fa_fwd_f32", "fa_get_device_status", "fa_status_string", "fa_last_error",
             "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_bytes", "fa_fwd_splitkv_suggest",
             "fa_fwd_host", "fa_fwd_host_workspace_bytes", "fa_selftest_wait_timeout", "fa_bwd",
-            "fa_bwd_workspace_bytes")
+            "fa_bwd_workspace_bytes", "fa_fwd_f32x3", "fa_fwd_f32x3_workspace_bytes")
 
 
 class FaError(RuntimeError):
@@ -77,6 +77,10 @@ def load_library():
         lib.fa_bwd.restype = ctypes.c_int
         lib.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64]
         lib.fa_bwd_workspace_bytes.restype = i64
+        lib.fa_fwd_f32x3.argtypes = [vp] * 5 + [i64] * 5 + [ctypes.c_float, ctypes.c_int, vp, i64, vp]
+        lib.fa_fwd_f32x3.restype = ctypes.c_int
+        lib.fa_fwd_f32x3_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.fa_fwd_f32x3_workspace_bytes.restype = i64
         lib.fa_selftest_wait_timeout.argtypes = [i64, vp]
         lib.fa_selftest_wait_timeout.restype = ctypes.c_int
         lib.fa_get_device_status.argtypes = [vp]
@@ -101,6 +105,18 @@ def fa_fwd_f32_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: 
                    scale: float, causal: bool, stream: int = 0) -> int:
     """Calls fa_fwd_f32 with raw device addresses; returns the status code."""
     return load_library().fa_fwd_f32(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
+
+
+def fa_fwd_f32x3_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
+                     scale: float, causal: bool, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Calls fa_fwd_f32x3 (fp32 on the tensor cores, three TF32 products)
+    with raw device addresses; returns the status code."""
+    return load_library().fa_fwd_f32x3(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)),
+                                       workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_f32x3_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return load_library().fa_fwd_f32x3_workspace_bytes(B, H, N, D)
 
 
 def fa_fwd_noalloc_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
@@ -240,6 +256,25 @@ def fa_fwd_f32(q, k, v, o, lse, scale: float, causal: bool = False, stream=None)
                             B, H, M, N, D, scale, causal, _stream_of(q, stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_f32")
+
+
+def fa_fwd_f32x3(q, k, v, o, lse, scale: float, causal: bool = False, workspace=None, stream=None) -> None:
+    """fp32 attention forward on the tensor cores (three TF32 products per
+    matrix product): writes ``o`` and ``lse``. ``workspace`` is a CUDA tensor
+    of at least fa_fwd_f32x3_workspace_bytes(B, H, N, D) bytes (allocated
+    here with torch when None)."""
+    import torch
+
+    B, H, M, N, D = _marshal(q, k, v, o, lse, torch.float32)
+    with torch.cuda.device(q.device):
+        need = fa_fwd_f32x3_workspace_bytes(B, H, N, D)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_f32x3_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, M, N, D, scale, causal, workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_of(q, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_f32x3")
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, scale: float, causal: bool = False, num_splits: int = 0,

@@ -255,6 +255,52 @@ FA_API fa_status fa_fwd_f32(const float* q, const float* k, const float* v, floa
     return FA_OK;
 }
 
+FA_API int64_t fa_fwd_f32x3_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
+    if (B < 0 || H < 0 || N < 0 || D < 0) return -1;
+    if (B > 0x7fffffff || H > 0x7fffffff || N > 0x7fffffff || D > 256) return -1;
+    return fa::x3_workspace_bytes(B * H, N, D);
+}
+
+FA_API fa_status fa_fwd_f32x3(const float* q, const float* k, const float* v, float* o, float* lse, int64_t B,
+                              int64_t H, int64_t M, int64_t N, int64_t D, float scale, int causal, void* workspace,
+                              int64_t workspace_bytes, void* stream) {
+    bool empty = false;
+    fa_status st = validate(q, k, v, o, lse, B, H, M, N, D, scale, 4, &empty);
+    if (st != FA_OK) return st;
+    if (D != 32 && D != 64 && D != 96 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "fa_fwd_f32x3 supports D in {32, 64, 96, 128} (got %lld)", (long long)D);
+    if (empty) return FA_OK;
+    const int64_t bh = B * H;
+    const int64_t need = fa_fwd_f32x3_workspace_bytes(B, H, N, D);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(FA_ERR_INVALID_ARG, "workspace of %lld bytes needed (got %lld)", (long long)need,
+                    (long long)workspace_bytes);
+    if (need > 0 && !aligned(workspace, 128)) return fail(FA_ERR_INVALID_ARG, "workspace must be 128-byte aligned");
+    const int64_t qb = bh * M * D * 4, kb = bh * N * D * 4;
+    if (overlaps(workspace, need, q, qb) || overlaps(workspace, need, k, kb) || overlaps(workspace, need, v, kb) ||
+        overlaps(workspace, need, o, qb) || overlaps(workspace, need, lse, bh * M * 4))
+        return fail(FA_ERR_INVALID_ARG, "workspace must not overlap the tensors");
+    uint32_t* word = nullptr;
+    if ((st = device_setup(false, &word)) != FA_OK) return st;
+    fa::X3Params p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.ws = static_cast<uint8_t*>(workspace);
+    p.err = word;
+    p.bh_count = static_cast<int>(bh);
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.D = static_cast<int>(D);
+    p.scale = scale;
+    p.causal = causal != 0;
+    const cudaError_t e = fa::launch_x3(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launching the fp32 tensor-core kernels");
+    return FA_OK;
+}
+
 FA_API fa_status fa_get_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

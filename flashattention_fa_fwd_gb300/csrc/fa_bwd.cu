@@ -11,13 +11,13 @@
 //   bwd_rowdot: Dl_i for every query row (one warp per row);
 //   bwd_dkdv:   one CTA per 64-key tile of one head; query rows stream through
 //               shared memory in chunks; dK and dV of the tile stay in
-//               registers (four threads per key, each holding a quarter of D);
+//               registers (eight threads per key, each holding an eighth of D);
 //   bwd_dq:     one CTA per 64-row query tile; key rows stream through shared
 //               memory; dQ stays in registers.
 // The two main kernels both rebuild P (and dP) -- seven products' worth of
 // work against the five of Practice 3 -- so that no output needs atomics and
-// the result is deterministic. The scores use exp2 with log2(e) folded into
-// the scale, as the forward does.
+// the result is deterministic. The scores use the hardware exp2 with log2(e)
+// folded into the scale, as the forward does.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,7 +31,7 @@ namespace fa {
 namespace {
 
 constexpr int kTile = 64;      // keys (dK/dV kernel) or query rows (dQ kernel) per CTA
-constexpr int kParts = 4;      // threads sharing one key or row, each over DV/4 of D
+constexpr int kParts = 8;      // threads sharing one key or row, each over DV/8 of D
 constexpr int kThreads = kTile * kParts;
 constexpr int kChunk = 32;     // rows streamed through shared memory per step
 constexpr float kLog2e = 1.4426950408889634f;
@@ -40,9 +40,16 @@ __device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) { return __bflo
 
 // Sum over the kParts consecutive lanes that share a key or row.
 __device__ __forceinline__ float part_sum(float x) {
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
+#pragma unroll
+    for (int off = 1; off < kParts; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
     return x;
+}
+
+// Hardware base-2 exponential (MUFU), as in the forward kernel.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __global__ void bwd_rowdot(const BwdParams p) {
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
             s = part_sum(s);
             dp = part_sum(dp);
             const bool vis = kvalid && row < p.M && (!p.causal || key <= row) && slse[i] != -INFINITY;
-            const float pr = vis ? exp2f(fmaf(s, cs, -slse[i] * kLog2e)) : 0.f;
+            const float pr = vis ? ex2(fmaf(s, cs, -slse[i] * kLog2e)) : 0.f;
             const float ds = pr * (dp - sdl[i]);
 #pragma unroll
             for (int c = 0; c < W; ++c) {
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dq(const BwdParams p) {
             s = part_sum(s);
             dp = part_sum(dp);
             const bool vis = rvalid && key < p.N && (!p.causal || key <= row) && lse != -INFINITY;
-            const float pr = vis ? exp2f(fmaf(s, cs, -lse * kLog2e)) : 0.f;
+            const float pr = vis ? ex2(fmaf(s, cs, -lse * kLog2e)) : 0.f;
             const float ds = pr * (dp - dl);
 #pragma unroll
             for (int c = 0; c < W; ++c) dq[c] = fmaf(ds, kj[c], dq[c]);

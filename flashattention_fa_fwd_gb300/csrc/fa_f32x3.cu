@@ -1,0 +1,496 @@
+// fp32 attention forward on the tensor cores: three TF32 products per matrix
+// product.
+//
+// "FlashAttention in Triton: A Tile-by-Tile Walkthrough" computes both dots of
+// its fp32 problem in IEEE fp32 on the CUDA cores and ends up slower than the
+// library kernel it is compared with. This path keeps the streaming softmax of
+// "FlashAttention-style kernel" (section "The loop") and moves the two
+// products onto tcgen05, which reads fp32 operands as TF32 (sign, exponent and
+// the top 10 of 23 mantissa bits). Every fp32 x is split as
+//   x = hi + lo,  hi = x rounded to 11 significant bits,  lo = x - hi (exact),
+// and a product A B is taken as  A_lo B_hi + A_hi B_lo + A_hi B_hi,  small
+// terms first, into an fp32 accumulator. The dropped A_lo B_lo term and the
+// truncation of lo to TF32 are each about 2^-22 relative to the product, so
+// the result is close to fp32 accuracy at a sixth of the bf16 tensor rate.
+//
+// Two kernels:
+//   x3_split: K and V, per 32-key block, into hi and lo images laid out as
+//             the MMA reads them (K-major, 128-byte swizzle: K as 32 keys x
+//             32-column panels, V transposed to D rows x 32 keys), so the
+//             attention kernel loads them with plain bulk copies.
+//   x3_fwd:   one CTA per 128-row query tile. The four softmax warps split
+//             their Q rows into tensor memory (the A operand of S = Q K^T),
+//             then run the online softmax one 32-key block at a time and
+//             hand P = hi + lo to the MMA through shared memory. One warp
+//             streams the K/V images through a ring, one thread issues the
+//             MMAs: S(j+1) is computed while the softmax works on S(j).
+// Masking (top-left causal, key tail), the safe max, the rare rescale of the
+// accumulator (only when a row's max grows by more than 2^8) and the final
+// division follow the bf16 kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int kBM = 128;              // query rows per CTA: one per softmax thread and TMEM lane
+constexpr int kBN = 32;               // keys per block: one 128-byte swizzle row of fp32
+constexpr int kThreads = 192;         // 4 softmax warps, the load warp, the MMA warp
+constexpr int kSplitThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // a row's reference max moves only when it grows by more
+
+// x = hi + lo with hi holding the 11 leading significant bits of x (rounded
+// to nearest, ties away from zero, on the magnitude) and lo the exact rest.
+// Finite inputs below 2^127 in magnitude.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    hi = __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+    lo = x - hi;
+}
+
+// Position (in floats) of element (row r, column c) inside one K-major,
+// 128-byte-swizzled panel of 32 fp32 columns: the 16-byte unit c / 4 of row
+// r is stored at unit (c / 4) xor (r mod 8).
+__host__ __device__ constexpr int swz(int r, int c) { return r * 32 + (((c >> 2) ^ (r & 7)) << 2) + (c & 3); }
+
+// K/V images of one 32-key block: [K hi | K lo | V^T hi | V^T lo], each
+// kBN * D floats. K parts: D/32 panels of 32 keys x 32 columns. V^T parts:
+// one panel of D rows x 32 keys.
+template <int D>
+__global__ void __launch_bounds__(kSplitThreads) x3_split(const float* __restrict__ k, const float* __restrict__ v,
+                                                          float* __restrict__ ws, int N, int nt) {
+    constexpr int HALF = kBN * D;
+    const int64_t blk = blockIdx.x;            // head * nt + key block
+    const int64_t head = blk / nt;
+    const int j = static_cast<int>(blk - head * nt);
+    const float* kh = k + head * N * D;
+    const float* vh = v + head * N * D;
+    float* out = ws + blk * (4 * HALF);
+    // K: one float4 of a key row per item; reads coalesce along the row.
+    constexpr int KU = D / 4;
+    for (int i = threadIdx.x; i < kBN * KU; i += kSplitThreads) {
+        const int r = i / KU, c = (i % KU) * 4;
+        const int key = j * kBN + r;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (key < N) x = *reinterpret_cast<const float4*>(kh + static_cast<int64_t>(key) * D + c);
+        float4 h, l;
+        split_tf32(x.x, h.x, l.x);
+        split_tf32(x.y, h.y, l.y);
+        split_tf32(x.z, h.z, l.z);
+        split_tf32(x.w, h.w, l.w);
+        const int dst = (c >> 5) * (kBN * 32) + swz(r, c & 31);
+        *reinterpret_cast<float4*>(out + dst) = h;
+        *reinterpret_cast<float4*>(out + HALF + dst) = l;
+    }
+    // V^T: four consecutive keys of one column d per item; d runs fastest
+    // across the threads so the reads of one key row coalesce.
+    for (int i = threadIdx.x; i < D * (kBN / 4); i += kSplitThreads) {
+        const int d = i % D, c = (i / D) * 4;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = j * kBN + c + e;
+            x[e] = key < N ? vh[static_cast<int64_t>(key) * D + d] : 0.f;
+        }
+        float4 h, l;
+        split_tf32(x[0], h.x, l.x);
+        split_tf32(x[1], h.y, l.y);
+        split_tf32(x[2], h.z, l.z);
+        split_tf32(x[3], h.w, l.w);
+        const int dst = swz(d, c);
+        *reinterpret_cast<float4*>(out + 2 * HALF + dst) = h;
+        *reinterpret_cast<float4*>(out + 3 * HALF + dst) = l;
+    }
+}
+
+template <int D>
+struct X3Cfg {
+    static constexpr int HALF = kBN * D * 4;                 // bytes of one K or V^T part
+    static constexpr int KV_BYTES = 4 * HALF;                // one ring stage: a key block's four parts
+    static constexpr int K_PANEL = kBN * 128;                // 32 keys x 128 B
+    static constexpr int P_HALF = kBM * 128;                 // P hi or lo: 128 rows x 32 keys
+    static constexpr int P_OFF = 0;
+    static constexpr int KV_OFF = 2 * P_HALF;
+    static constexpr int NS_FIT = (232448 - 1024 - 512 - KV_OFF) / KV_BYTES;
+    // D <= 64: two stages, so that two CTAs share an SM.
+    static constexpr int NS = (D <= 64) ? 2 : (NS_FIT < 4 ? NS_FIT : 4);
+    static constexpr int BAR_OFF = KV_OFF + NS * KV_BYTES;
+    static constexpr int FULL = 0, EMPTY = NS, Q_READY = 2 * NS, S_FULL = Q_READY + 1, S_FREE = S_FULL + 2;
+    static constexpr int P_FULL = S_FREE + 2, O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, NUM_BARS = DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tensor-memory base, abort flag
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024 B
+    // Tensor-memory columns: Q hi, Q lo, O, two S buffers.
+    static constexpr uint32_t QH = 0, QL = D, OC = 2 * D, SC0 = 3 * D, SC1 = 3 * D + kBN;
+    static constexpr uint32_t TMEM_COLS = (3 * D + 2 * kBN <= 256) ? 256 : 512;
+    static_assert(D % 32 == 0 && D >= 32 && D <= 128, "D");
+    static_assert(NS >= 2, "ring stages");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Per-CTA view of the barriers and the abort flag.
+struct X3Ctx {
+    uint32_t bar0;
+    volatile int* abort;
+    uint32_t* err;
+    __device__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
+    __device__ bool wait(int i, int parity) const { return mbar_wait(bar(i), static_cast<uint32_t>(parity) & 1u, abort, err); }
+    // Warp-uniform result, for code that runs warp-collective tcgen05 loads next.
+    __device__ bool wait_warp(int i, int parity) const { return __all_sync(0xffffffffu, wait(i, parity)); }
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// ------------------------------------------------------------ softmax warps
+// Thread t of warps 0-3 owns query row r0 + t and tensor-memory lane t.
+template <int D>
+__device__ __forceinline__ void x3_softmax(const X3Params& p, const X3Ctx& c, uint32_t s0, uint32_t tmem, int bh,
+                                           int r0, int nb) {
+    using C = X3Cfg<D>;
+    const int t = threadIdx.x;
+    const int row = r0 + t;
+    const bool in = row < p.M;
+    const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
+    const int64_t row_off = (static_cast<int64_t>(bh) * p.M + row) * D;
+    // Q row -> hi and lo parts in tensor memory (rows past M are zero).
+    if (nb > 0) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (in) x = *reinterpret_cast<const float4*>(p.q + row_off + cc * 32 + i * 4);
+                const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float h, l;
+                    split_tf32(xs[e], h, l);
+                    hi[i * 4 + e] = __float_as_uint(h);
+                    lo[i * 4 + e] = __float_as_uint(l);
+                }
+            }
+            tmem_st_x32(tm + C::QH + cc * 32, hi);
+            tmem_st_x32(tm + C::QL + cc * 32, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(c.bar(C::Q_READY));
+    }
+    const float cs = p.scale * kLog2e;
+    const int lim = p.causal ? min(p.N, row + 1) : p.N;   // keys [0, lim) are visible
+    const uint32_t prow = s0 + C::P_OFF + t * 128;
+    const uint32_t sw = t & 7;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+#pragma unroll 1
+    for (int j = 0; j < nb; ++j) {
+        const int sb = j & 1;
+        if (!c.wait_warp(C::S_FULL + sb, j >> 1)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld_x32(tm + (sb ? C::SC1 : C::SC0), sr);
+        tmem_ld_wait(sr);
+        tc_fence_before();
+        mbar_arrive(c.bar(C::S_FREE + sb));
+        const int key0 = j * kBN;
+        float x[32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            x[i] = (key0 + i < lim) ? __uint_as_float(sr[i]) * cs : -INFINITY;
+            mx = fmaxf(mx, x[i]);
+        }
+        float m_new = m_ref;
+        bool resc = false;
+        if (mx > m_ref + kRescaleLog2) {
+            m_new = mx;
+            resc = j > 0;
+        }
+        const float m_s = (m_new == -INFINITY) ? 0.f : m_new;
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            x[i] = ex2(x[i] - m_s);
+            sum += x[i];
+        }
+        const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+        l = l * alpha + sum;
+        // P V of the previous block has completed: O is final for it and
+        // the P buffer is free.
+        if (j > 0) {
+            if (!c.wait_warp(C::O_DONE, j - 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, resc)) {   // the warp rescales together; alpha = 1 leaves a row as it is
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld_x32(tm + C::OC + cc * 32, o);
+                tmem_ld_wait(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st_x32(tm + C::OC + cc * 32, o);
+            }
+            tmem_st_wait();
+        }
+        // P = hi + lo into row t of the two shared-memory operand panels.
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float h[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_tf32(x[u * 4 + e], h[e], lo[e]);
+            const uint32_t a = prow + ((static_cast<uint32_t>(u) ^ sw) << 4);
+            st_shared_v4(a, h[0], h[1], h[2], h[3]);
+            st_shared_v4(a + C::P_HALF, lo[0], lo[1], lo[2], lo[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(c.bar(C::P_FULL));
+        m_ref = m_new;
+    }
+    if (ok && nb > 0) {
+        ok = c.wait_warp(C::O_DONE, nb - 1);
+        tc_fence_after();
+    }
+    if (!ok) return;
+    // Epilogue: O = acc / l, LSE = ln 2 * m + ln l (natural log of the
+    // scaled scores' exponential sum); a row that saw no key gets O = 0 and
+    // LSE = -inf.
+    float* orow = p.o + row_off;
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        if (nb > 0) {
+            tmem_ld_x32(tm + C::OC + cc * 32, o);
+            tmem_ld_wait(o);
+        }
+        if (in) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (nb > 0 && l > 0.f) {
+                    w.x = __uint_as_float(o[i * 4 + 0]) / l;
+                    w.y = __uint_as_float(o[i * 4 + 1]) / l;
+                    w.z = __uint_as_float(o[i * 4 + 2]) / l;
+                    w.w = __uint_as_float(o[i * 4 + 3]) / l;
+                }
+                *reinterpret_cast<float4*>(orow + cc * 32 + i * 4) = w;
+            }
+        }
+    }
+    if (in) p.lse[static_cast<int64_t>(bh) * p.M + row] = (nb > 0 && l > 0.f) ? m_ref * kLn2 + logf(l) : -INFINITY;
+}
+
+// ---------------------------------------------------------------- load warp
+template <int D>
+__device__ __forceinline__ void x3_producer(const X3Params& p, const X3Ctx& c, uint32_t s0, int bh, int nb, int nt) {
+    using C = X3Cfg<D>;
+    const uint8_t* img = p.ws + static_cast<int64_t>(bh) * nt * C::KV_BYTES;
+    int issued = 0;
+#pragma unroll 1
+    for (int j = 0; j < nb; ++j) {
+        const int st = j % C::NS;
+        if (j >= C::NS && !c.wait(C::EMPTY + st, j / C::NS - 1)) break;
+        const uint32_t dst = s0 + C::KV_OFF + st * C::KV_BYTES;
+        const uint8_t* src = img + static_cast<int64_t>(j) * C::KV_BYTES;
+        mbar_arrive_expect_tx(c.bar(C::FULL + st), C::KV_BYTES);
+#pragma unroll
+        for (int part = 0; part < 4; ++part) bulk_load(dst + part * C::HALF, src + part * C::HALF, C::HALF, c.bar(C::FULL + st));
+        ++issued;
+    }
+    // Every copy issued lands before the CTA's shared memory is released.
+    for (int s = 0; s < C::NS && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / C::NS) * C::NS;
+        mbar_wait_drain(c.bar(C::FULL + s), (last / C::NS) & 1);
+    }
+}
+
+// --------------------------------------------------------------- MMA thread
+template <int D>
+__device__ __forceinline__ void x3_mma(const X3Ctx& c, uint32_t s0, uint32_t tmem, int nb) {
+    using C = X3Cfg<D>;
+    constexpr uint32_t id_s = idesc_tf32_f32(kBM, kBN);
+    constexpr uint32_t id_o = idesc_tf32_f32(kBM, D);
+    // Descriptor template with a zero start address; adding (address >> 4)
+    // fills the 14-bit start field. K-major, 128-byte swizzle: SBO = 8 rows
+    // of 128 B; an 8-column (32-byte) K-step advances the start by 2.
+    const uint64_t dz = smem_desc_sw128(0, 16, 1024);
+    constexpr uint32_t kPanel = C::K_PANEL >> 4;
+    // S(j) = Q_lo K_hi^T + Q_hi K_lo^T + Q_hi K_hi^T, Q from tensor memory.
+    auto issue_s = [&](int j) -> bool {
+        const int st = j % C::NS, sb = j & 1;
+        if (!c.wait(C::FULL + st, j / C::NS)) return false;
+        if (j >= 2 && !c.wait(C::S_FREE + sb, (j >> 1) - 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = s0 + C::KV_OFF + st * C::KV_BYTES;
+        const uint64_t dkh = dz + (kb >> 4), dkl = dz + ((kb + C::HALF) >> 4);
+        const uint32_t scol = tmem + (sb ? C::SC1 : C::SC0);
+#pragma unroll
+        for (int kk = 0; kk < D / 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+            mma_ts_tf32(scol, tmem + C::QL + kk * 8, dkh + off, id_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+            mma_ts_tf32(scol, tmem + C::QH + kk * 8, dkl + off, id_s, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 2;
+            mma_ts_tf32(scol, tmem + C::QH + kk * 8, dkh + off, id_s, 1u);
+        }
+        mma_commit(c.bar(C::S_FULL + sb));
+        return true;
+    };
+    // O (+)= P_lo V_hi + P_hi V_lo + P_hi V_hi, P from shared memory, V^T
+    // K-major; the first product of the tile overwrites O.
+    auto issue_pv = [&](int j) -> bool {
+        const int st = j % C::NS;
+        if (!c.wait(C::P_FULL, j)) return false;
+        tc_fence_after();
+        const uint32_t vb = s0 + C::KV_OFF + st * C::KV_BYTES + 2 * C::HALF;
+        const uint64_t dvh = dz + (vb >> 4), dvl = dz + ((vb + C::HALF) >> 4);
+        const uint64_t dph = dz + ((s0 + C::P_OFF) >> 4), dpl = dz + ((s0 + C::P_OFF + C::P_HALF) >> 4);
+        const uint32_t ocol = tmem + C::OC;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 8; ++kk) mma_ss_tf32(ocol, dpl + kk * 2, dvh + kk * 2, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 8; ++kk) mma_ss_tf32(ocol, dph + kk * 2, dvl + kk * 2, id_o, 1u);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 8; ++kk) mma_ss_tf32(ocol, dph + kk * 2, dvh + kk * 2, id_o, 1u);
+        mma_commit(c.bar(C::O_DONE));
+        mma_commit(c.bar(C::EMPTY + st));
+        return true;
+    };
+    bool ok = nb > 0 && c.wait(C::Q_READY, 0);
+    if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+    }
+#pragma unroll 1
+    for (int j = 0; ok && j < nb; ++j) {
+        if (j + 1 < nb && !issue_s(j + 1)) break;
+        ok = issue_pv(j);
+    }
+    // Every MMA issued completes before tensor or shared memory is released.
+    mma_commit(c.bar(C::DRAIN));
+    mbar_wait_drain(c.bar(C::DRAIN), 0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) x3_fwd(const X3Params p) {
+    using C = X3Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(sm);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+    X3Ctx c;
+    c.bar0 = s0 + C::BAR_OFF;
+    c.abort = reinterpret_cast<volatile int*>(misc + 1);
+    c.err = p.err;
+    const int warp = threadIdx.x / 32;
+    // Heaviest query tiles (the last ones, under the causal mask) first.
+    const int mtiles = (p.M + kBM - 1) / kBM;
+    const int mt = mtiles - 1 - static_cast<int>(blockIdx.x / p.bh_count);
+    const int bh = static_cast<int>(blockIdx.x % p.bh_count);
+    const int r0 = mt * kBM;
+    const int kend = p.causal ? min(p.N, min(p.M, r0 + kBM)) : p.N;
+    const int nb = (kend + kBN - 1) / kBN;
+    const int nt = (p.N + kBN - 1) / kBN;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(c.bar(C::FULL + i), 1);
+            mbar_init(c.bar(C::EMPTY + i), 1);
+        }
+        mbar_init(c.bar(C::Q_READY), kBM);
+        mbar_init(c.bar(C::S_FULL + 0), 1);
+        mbar_init(c.bar(C::S_FULL + 1), 1);
+        mbar_init(c.bar(C::S_FREE + 0), kBM);
+        mbar_init(c.bar(C::S_FREE + 1), kBM);
+        mbar_init(c.bar(C::P_FULL), kBM);
+        mbar_init(c.bar(C::O_DONE), 1);
+        mbar_init(c.bar(C::DRAIN), 1);
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(misc), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    if (warp < 4) {
+        x3_softmax<D>(p, c, s0, tmem, bh, r0, nb);
+    } else if (warp == 4) {
+        if ((threadIdx.x & 31) == 0) x3_producer<D>(p, c, s0, bh, nb, nt);
+    } else if ((threadIdx.x & 31) == 0) {
+        x3_mma<D>(c, s0, tmem, nb);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_x3_t(const X3Params& p, cudaStream_t s) {
+    using C = X3Cfg<D>;
+    const int64_t nt = (static_cast<int64_t>(p.N) + kBN - 1) / kBN;
+    const int64_t split_blocks = static_cast<int64_t>(p.bh_count) * nt;
+    const int64_t blocks = static_cast<int64_t>(p.bh_count) * ((static_cast<int64_t>(p.M) + kBM - 1) / kBM);
+    if (split_blocks > 0x7fffffffLL || blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (split_blocks > 0) {
+        x3_split<D><<<static_cast<unsigned>(split_blocks), kSplitThreads, 0, s>>>(p.k, p.v, reinterpret_cast<float*>(p.ws),
+                                                                                 p.N, static_cast<int>(nt));
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(x3_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    x3_fwd<D><<<static_cast<unsigned>(blocks), kThreads, C::SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t x3_workspace_bytes(int64_t bh, int64_t N, int64_t D) {
+    const int64_t nt = (N + kBN - 1) / kBN;
+    return bh * nt * 4 * kBN * D * static_cast<int64_t>(sizeof(float));
+}
+
+cudaError_t launch_x3(const X3Params& p, cudaStream_t s) {
+    switch (p.D) {
+        case 32: return launch_x3_t<32>(p, s);
+        case 64: return launch_x3_t<64>(p, s);
+        case 96: return launch_x3_t<96>(p, s);
+        case 128: return launch_x3_t<128>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

@@ -82,6 +82,30 @@ struct BwdParams {
 // Launches the three backward kernels (row dots, dK/dV, dQ) on `s`.
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s);
 
+// Arguments of the fp32 tensor-core path (three TF32 products per matrix
+// product): fp32 Q, K, V in, fp32 O and LSE out.
+struct X3Params {
+    const float* q;   // [BH, M, D]
+    const float* k;   // [BH, N, D]
+    const float* v;   // [BH, N, D]
+    float* o;         // [BH, M, D]
+    float* lse;       // [BH, M]
+    uint8_t* ws;      // K and V split into TF32 hi/lo parts, 32-key tile images (x3_workspace_bytes)
+    uint32_t* err;    // device status word
+    int bh_count;
+    int M;
+    int N;
+    int D;            // 32, 64, 96 or 128
+    float scale;
+    int causal;
+};
+
+// Bytes of the K/V image workspace for B*H heads of N keys of width D.
+int64_t x3_workspace_bytes(int64_t bh, int64_t N, int64_t D);
+
+// Launches the split pre-pass and the attention kernel on `s`.
+cudaError_t launch_x3(const X3Params& p, cudaStream_t s);
+
 // Merges split-KV partial results: for every row, LSE = ln sum_s exp(LSE_s)
 // and O = sum_s exp(LSE_s - LSE) O_s, written as bf16 O and fp32 LSE.
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, void* o, float* lse, int64_t rows, int D,

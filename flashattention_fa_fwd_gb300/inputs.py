@@ -65,6 +65,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("cross_b2_h8_m1000_n3000_d96_peaked", 4, 2, 8, 1000, 3000, 96,
              "bf16", False, sigma_qk=3.0),
     Workload("long_causal_b1_h8_s65536_d64", 5, 1, 8, 65536, 65536, 64, "bf16", True),
+    # The GPT-2-medium and causal 4K shapes in fp32, for the fp32 paths.
+    Workload("f32_gpt2m_b64_h16_s1024_d64", 6, 64, 16, 1024, 1024, 64, "f32", False),
+    Workload("f32_causal_b8_h32_s4096_d128", 7, 8, 32, 4096, 4096, 128, "f32", True),
 ]}
 
 

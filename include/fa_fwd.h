@@ -112,6 +112,38 @@ fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, f
                      float scale, int causal, void* stream);
 
 /*
+ * fp32 attention forward on the tensor cores: the result of fa_fwd_f32 (same
+ * arguments, layouts and semantics) with both matrix products on tcgen05 as
+ * three TF32 products. Every fp32 input x is split as x = hi + lo, hi = x
+ * rounded to 11 significant bits, lo = x - hi, and a product A B is taken as
+ * A_lo B_hi + A_hi B_lo + A_hi B_hi in fp32: near-fp32 accuracy (the dropped
+ * A_lo B_lo term is ~2^-22 of the product) where fa_fwd_f32's exact FMAs are
+ * CUDA-core bound. This is the fast fp32 path that "FlashAttention in
+ * Triton: A Tile-by-Tile Walkthrough" lacks: its IEEE-fp32 kernel ends up
+ * slower than the library attention it is compared with.
+ *
+ *   q, k, v, o, lse  as fa_fwd_f32 (fp32, contiguous, 16-byte aligned; lse 4)
+ *   D                32, 64, 96 or 128 (others: FA_ERR_UNSUPPORTED)
+ *   workspace        device memory owned by the caller, 128-byte aligned, at
+ *                    least fa_fwd_f32x3_workspace_bytes(B, H, N, D) bytes;
+ *                    receives K and V split into hi/lo tile images (it may
+ *                    be null when that size is 0, i.e. N = 0)
+ *
+ * Inputs must be finite and below 2^127 in magnitude. Asynchronous on
+ * `stream`: two kernels (the split, then the attention), never
+ * synchronises. Errors: fa_fwd_f32's checks, plus FA_ERR_INVALID_ARG for a
+ * missing, short or misaligned workspace or one that overlaps a tensor;
+ * device wait timeouts surface through fa_get_device_status.
+ */
+fa_status fa_fwd_f32x3(const float* q, const float* k, const float* v, float* o, float* lse,
+                       int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
+                       float scale, int causal, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_f32x3 needs: 16 bytes per (head, key, column) with
+ * the keys padded to a multiple of 32 (-1 for negative sizes). Needs no GPU. */
+int64_t fa_fwd_f32x3_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
+
+/*
  * Split-KV bf16 forward: the same result as fa_fwd (same arguments, layouts
  * and checks), computed by cutting each query tile's keys into `num_splits`
  * contiguous ranges that different CTAs process in parallel, then merging

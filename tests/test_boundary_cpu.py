@@ -171,3 +171,21 @@ def test_bwd_workspace_size_and_checks(lib):
     assert fa.fa_bwd_raw(*PTRS, 9 * A, 6 * A, 6 * A, 8 * A, 1, 2, 256, 512, 64, 0.125, False, W, need, 0) \
         == fa.FA_ERR_INVALID_ARG                                                  # dq overlaps dk
     assert fa.fa_bwd_raw(*PTRS, 9 * A, *grads, 0, 2, 256, 512, 64, 0.125, False, 0, 0, 0) == fa.FA_OK  # empty
+
+
+def test_f32x3_workspace_size_and_checks(lib):
+    # 16 bytes per (head, key, column), keys padded to a multiple of 32.
+    assert fa.fa_fwd_f32x3_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 64 * 16
+    assert fa.fa_fwd_f32x3_workspace_bytes(1, 1, 0, 64) == 0
+    assert fa.fa_fwd_f32x3_workspace_bytes(-1, 1, 1, 64) == -1
+    W = 64 * A
+    need = fa.fa_fwd_f32x3_workspace_bytes(1, 2, 512, 64)
+    args = (*PTRS, 1, 2, 256, 512, 64, 0.125, False)
+    assert fa.fa_fwd_f32x3_raw(*args, 0, need, 0) == fa.FA_ERR_INVALID_ARG          # missing workspace
+    assert fa.fa_fwd_f32x3_raw(*args, W, need - 16, 0) == fa.FA_ERR_INVALID_ARG     # short workspace
+    assert fa.fa_fwd_f32x3_raw(*args, W + 16, need, 0) == fa.FA_ERR_INVALID_ARG     # misaligned workspace
+    assert fa.fa_fwd_f32x3_raw(*args, A, need, 0) == fa.FA_ERR_INVALID_ARG          # overlaps q
+    for D in (8, 48, 80, 112, 256):
+        assert fa.fa_fwd_f32x3_raw(*PTRS, 1, 2, 256, 512, D, 0.125, False, W, 1 << 30, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_f32x3_raw(*PTRS, 1, 2, 256, 512, 64, float("nan"), False, W, need, 0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_f32x3_raw(*PTRS, 0, 2, 256, 512, 64, 0.125, False, 0, 0, 0) == fa.FA_OK  # empty
