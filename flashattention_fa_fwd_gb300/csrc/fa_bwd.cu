@@ -11,7 +11,8 @@
 //   bwd_rowdot: Dl_i for every query row (one warp per row);
 //   bwd_dkdv:   one CTA per 64-key tile of one head; query rows stream through
 //               shared memory in chunks; dK and dV of the tile stay in
-//               registers (eight threads per key, each holding an eighth of D);
+//               registers (eight threads per key at D = 128, four below,
+//               each holding its share of D);
 //   bwd_dq:     one CTA per 64-row query tile; key rows stream through shared
 //               memory; dQ stays in registers.
 // The two main kernels both rebuild P (and dP) -- seven products' worth of
@@ -31,17 +32,22 @@ namespace fa {
 namespace {
 
 constexpr int kTile = 64;      // keys (dK/dV kernel) or query rows (dQ kernel) per CTA
-constexpr int kParts = 8;      // threads sharing one key or row, each over DV/8 of D
-constexpr int kThreads = kTile * kParts;
+// Threads sharing one key or row, each over DV / parts of D: eight at D = 128
+// (fewer registers, twice the warps), four below (fewer shuffles).
+template <int DV>
+__host__ __device__ constexpr int parts() { return DV >= 128 ? 8 : 4; }
+template <int DV>
+__host__ __device__ constexpr int threads() { return kTile * parts<DV>(); }
 constexpr int kChunk = 32;     // rows streamed through shared memory per step
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// Sum over the kParts consecutive lanes that share a key or row.
+// Sum over the P consecutive lanes that share a key or row.
+template <int P>
 __device__ __forceinline__ float part_sum(float x) {
 #pragma unroll
-    for (int off = 1; off < kParts; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    for (int off = 1; off < P; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
     return x;
 }
 
@@ -70,21 +76,22 @@ __global__ void bwd_rowdot(const BwdParams p) {
 // columns >= D.
 template <int DV>
 __device__ __forceinline__ void stage(float* dst, const __nv_bfloat16* src, int r0, int limit, int D) {
-    for (int i = threadIdx.x; i < kChunk * DV; i += kThreads) {
+    for (int i = threadIdx.x; i < kChunk * DV; i += threads<DV>()) {
         const int r = i / DV, c = i % DV;
         dst[i] = (r0 + r < limit && c < D) ? ld_bf16(src + static_cast<int64_t>(r0 + r) * D + c) : 0.f;
     }
 }
 
 template <int DV>
-__global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
-    constexpr int W = DV / kParts;
+__global__ void __launch_bounds__(threads<DV>()) bwd_dkdv(const BwdParams p) {
+    constexpr int P = parts<DV>();
+    constexpr int W = DV / P;
     __shared__ float sq[kChunk * DV], sdo[kChunk * DV], slse[kChunk], sdl[kChunk];
     const int tiles = (p.N + kTile - 1) / kTile;
     const int bh = blockIdx.x / tiles;
     const int key0 = (blockIdx.x - bh * tiles) * kTile;
-    const int key = key0 + threadIdx.x / kParts;
-    const int c0 = (threadIdx.x % kParts) * W;            // this thread's columns [c0, c0 + W)
+    const int key = key0 + threadIdx.x / P;
+    const int c0 = (threadIdx.x % P) * W;            // this thread's columns [c0, c0 + W)
     const bool kvalid = key < p.N;
     const int64_t kv_base = static_cast<int64_t>(bh) * p.N * p.D;
     const int64_t q_base = static_cast<int64_t>(bh) * p.M * p.D;
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
         __syncthreads();
         stage<DV>(sq, p.q + q_base, r0, p.M, p.D);
         stage<DV>(sdo, p.dout + q_base, r0, p.M, p.D);
-        for (int i = threadIdx.x; i < kChunk; i += kThreads) {
+        for (int i = threadIdx.x; i < kChunk; i += threads<DV>()) {
             const bool in = r0 + i < p.M;
             const int64_t row = static_cast<int64_t>(bh) * p.M + r0 + i;
             slse[i] = in ? p.lse[row] : -INFINITY;
@@ -121,8 +128,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
                 s = fmaf(kr[c], qi[c], s);
                 dp = fmaf(vr[c], doi[c], dp);
             }
-            s = part_sum(s);
-            dp = part_sum(dp);
+            s = part_sum<P>(s);
+            dp = part_sum<P>(dp);
             const bool vis = kvalid && row < p.M && (!p.causal || key <= row) && slse[i] != -INFINITY;
             const float pr = vis ? ex2(fmaf(s, cs, -slse[i] * kLog2e)) : 0.f;
             const float ds = pr * (dp - sdl[i]);
@@ -145,14 +152,15 @@ __global__ void __launch_bounds__(kThreads) bwd_dkdv(const BwdParams p) {
 }
 
 template <int DV>
-__global__ void __launch_bounds__(kThreads) bwd_dq(const BwdParams p) {
-    constexpr int W = DV / kParts;
+__global__ void __launch_bounds__(threads<DV>()) bwd_dq(const BwdParams p) {
+    constexpr int P = parts<DV>();
+    constexpr int W = DV / P;
     __shared__ float sk[kChunk * DV], sv[kChunk * DV];
     const int tiles = (p.M + kTile - 1) / kTile;
     const int bh = blockIdx.x / tiles;
     const int row0 = (blockIdx.x - bh * tiles) * kTile;
-    const int row = row0 + threadIdx.x / kParts;
-    const int c0 = (threadIdx.x % kParts) * W;
+    const int row = row0 + threadIdx.x / P;
+    const int c0 = (threadIdx.x % P) * W;
     const bool rvalid = row < p.M;
     const int64_t q_base = static_cast<int64_t>(bh) * p.M * p.D;
     const int64_t kv_base = static_cast<int64_t>(bh) * p.N * p.D;
@@ -184,8 +192,8 @@ __global__ void __launch_bounds__(kThreads) bwd_dq(const BwdParams p) {
                 s = fmaf(qr[c], kj[c], s);
                 dp = fmaf(dor[c], vj[c], dp);
             }
-            s = part_sum(s);
-            dp = part_sum(dp);
+            s = part_sum<P>(s);
+            dp = part_sum<P>(dp);
             const bool vis = rvalid && key < p.N && (!p.causal || key <= row) && lse != -INFINITY;
             const float pr = vis ? ex2(fmaf(s, cs, -lse * kLog2e)) : 0.f;
             const float ds = pr * (dp - dl);
@@ -205,10 +213,10 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
     const int64_t kv_blocks = static_cast<int64_t>(p.bh_count) * ((p.N + kTile - 1) / kTile);
     const int64_t q_blocks = static_cast<int64_t>(p.bh_count) * ((p.M + kTile - 1) / kTile);
     if (kv_blocks > 0x7fffffffLL || q_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (kv_blocks > 0) bwd_dkdv<DV><<<static_cast<unsigned>(kv_blocks), kThreads, 0, s>>>(p);
+    if (kv_blocks > 0) bwd_dkdv<DV><<<static_cast<unsigned>(kv_blocks), threads<DV>(), 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq<DV><<<static_cast<unsigned>(q_blocks), kThreads, 0, s>>>(p);
+    bwd_dq<DV><<<static_cast<unsigned>(q_blocks), threads<DV>(), 0, s>>>(p);
     return cudaGetLastError();
 }
 

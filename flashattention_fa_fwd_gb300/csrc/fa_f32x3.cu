@@ -21,9 +21,11 @@
 //   x3_fwd:   one CTA per 128-row query tile. The four softmax warps split
 //             their Q rows into tensor memory (the A operand of S = Q K^T),
 //             then run the online softmax one 32-key block at a time and
-//             hand P = hi + lo to the MMA through shared memory. One warp
-//             streams the K/V images through a ring, one thread issues the
-//             MMAs: S(j+1) is computed while the softmax works on S(j).
+//             hand P = hi + lo to the MMA through shared memory. Two warps
+//             stream the K and the V images through rings of their own (a K
+//             slot is free again as soon as its S product completes, so K
+//             runs several blocks ahead), one thread issues the MMAs: S(j+1)
+//             is computed while the softmax works on S(j).
 // Masking (top-left causal, key tail), the safe max, the rare rescale of the
 // accumulator (only when a row's max grows by more than 2^8) and the final
 // division follow the bf16 kernel.
@@ -42,7 +44,7 @@ namespace {
 
 constexpr int kBM = 128;              // query rows per CTA: one per softmax thread and TMEM lane
 constexpr int kBN = 32;               // keys per block: one 128-byte swizzle row of fp32
-constexpr int kThreads = 192;         // 4 softmax warps, the load warp, the MMA warp
+constexpr int kThreads = 224;         // 4 softmax warps, the K load warp, the MMA warp, the V load warp
 constexpr int kSplitThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -113,17 +115,19 @@ __global__ void __launch_bounds__(kSplitThreads) x3_split(const float* __restric
 
 template <int D>
 struct X3Cfg {
-    static constexpr int HALF = kBN * D * 4;                 // bytes of one K or V^T part
-    static constexpr int KV_BYTES = 4 * HALF;                // one ring stage: a key block's four parts
+    static constexpr int HALF = kBN * D * 4;                 // bytes of one K or V^T part (hi or lo)
+    static constexpr int SLOT = 2 * HALF;                    // one ring slot: hi and lo of K, or of V^T
     static constexpr int K_PANEL = kBN * 128;                // 32 keys x 128 B
     static constexpr int P_HALF = kBM * 128;                 // P hi or lo: 128 rows x 32 keys
     static constexpr int P_OFF = 0;
-    static constexpr int KV_OFF = 2 * P_HALF;
-    static constexpr int NS_FIT = (232448 - 1024 - 512 - KV_OFF) / KV_BYTES;
-    // D <= 64: two stages, so that two CTAs share an SM.
+    static constexpr int K_OFF = 2 * P_HALF;
+    static constexpr int NS_FIT = (232448 - 1024 - 512 - K_OFF) / (2 * SLOT);
+    // Slots per ring (K and V alike). D <= 64: two, so that two CTAs share an SM.
     static constexpr int NS = (D <= 64) ? 2 : (NS_FIT < 4 ? NS_FIT : 4);
-    static constexpr int BAR_OFF = KV_OFF + NS * KV_BYTES;
-    static constexpr int FULL = 0, EMPTY = NS, Q_READY = 2 * NS, S_FULL = Q_READY + 1, S_FREE = S_FULL + 2;
+    static constexpr int V_OFF = K_OFF + NS * SLOT;
+    static constexpr int BAR_OFF = V_OFF + NS * SLOT;
+    static constexpr int K_FULL = 0, K_EMPTY = NS, V_FULL = 2 * NS, V_EMPTY = 3 * NS, Q_READY = 4 * NS;
+    static constexpr int S_FULL = Q_READY + 1, S_FREE = S_FULL + 2;
     static constexpr int P_FULL = S_FREE + 2, O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, NUM_BARS = DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tensor-memory base, abort flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024 B
@@ -131,7 +135,7 @@ struct X3Cfg {
     static constexpr uint32_t QH = 0, QL = D, OC = 2 * D, SC0 = 3 * D, SC1 = 3 * D + kBN;
     static constexpr uint32_t TMEM_COLS = (3 * D + 2 * kBN <= 256) ? 256 : 512;
     static_assert(D % 32 == 0 && D >= 32 && D <= 128, "D");
-    static_assert(NS >= 2, "ring stages");
+    static_assert(NS >= 2, "ring slots");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -145,6 +149,28 @@ struct X3Ctx {
     // Warp-uniform result, for code that runs warp-collective tcgen05 loads next.
     __device__ bool wait_warp(int i, int parity) const { return __all_sync(0xffffffffu, wait(i, parity)); }
 };
+
+// Pairwise reductions over a row's 32 values (short dependency chains).
+__device__ __forceinline__ float tree_max(const float (&x)[32]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(x[i], x[i + 16]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+__device__ __forceinline__ float tree_sum(const float (&x)[32]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = x[i] + x[i + 16];
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] += m[i + w];
+    return m[0];
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
@@ -207,12 +233,14 @@ __device__ __forceinline__ void x3_softmax(const X3Params& p, const X3Ctx& c, ui
         mbar_arrive(c.bar(C::S_FREE + sb));
         const int key0 = j * kBN;
         float x[32];
-        float mx = -INFINITY;
+        if (key0 + kBN <= lim) {   // every key of the block visible to this row
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            x[i] = (key0 + i < lim) ? __uint_as_float(sr[i]) * cs : -INFINITY;
-            mx = fmaxf(mx, x[i]);
+            for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(sr[i]) * cs;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = (key0 + i < lim) ? __uint_as_float(sr[i]) * cs : -INFINITY;
         }
+        float mx = tree_max(x);
         float m_new = m_ref;
         bool resc = false;
         if (mx > m_ref + kRescaleLog2) {
@@ -220,12 +248,9 @@ __device__ __forceinline__ void x3_softmax(const X3Params& p, const X3Ctx& c, ui
             resc = j > 0;
         }
         const float m_s = (m_new == -INFINITY) ? 0.f : m_new;
-        float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            x[i] = ex2(x[i] - m_s);
-            sum += x[i];
-        }
+        for (int i = 0; i < 32; ++i) x[i] = ex2(x[i] - m_s);
+        const float sum = tree_sum(x);
         const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
         l = l * alpha + sum;
         // P V of the previous block has completed: O is final for it and
@@ -297,27 +322,31 @@ __device__ __forceinline__ void x3_softmax(const X3Params& p, const X3Ctx& c, ui
     if (in) p.lse[static_cast<int64_t>(bh) * p.M + row] = (nb > 0 && l > 0.f) ? m_ref * kLn2 + logf(l) : -INFINITY;
 }
 
-// ---------------------------------------------------------------- load warp
+// -------------------------------------------------------------- load warps
+// Streams one half of every key block's image (part 0: K hi and lo; part 1:
+// V^T hi and lo) through its ring of NS slots.
 template <int D>
-__device__ __forceinline__ void x3_producer(const X3Params& p, const X3Ctx& c, uint32_t s0, int bh, int nb, int nt) {
+__device__ __forceinline__ void x3_producer(const X3Params& p, const X3Ctx& c, uint32_t s0, int bh, int nb, int nt,
+                                            int part) {
     using C = X3Cfg<D>;
-    const uint8_t* img = p.ws + static_cast<int64_t>(bh) * nt * C::KV_BYTES;
+    const int full = part ? C::V_FULL : C::K_FULL, empty = part ? C::V_EMPTY : C::K_EMPTY;
+    const uint32_t ring = s0 + (part ? C::V_OFF : C::K_OFF);
+    const uint8_t* img = p.ws + static_cast<int64_t>(bh) * nt * (2 * C::SLOT) + part * C::SLOT;
     int issued = 0;
 #pragma unroll 1
     for (int j = 0; j < nb; ++j) {
         const int st = j % C::NS;
-        if (j >= C::NS && !c.wait(C::EMPTY + st, j / C::NS - 1)) break;
-        const uint32_t dst = s0 + C::KV_OFF + st * C::KV_BYTES;
-        const uint8_t* src = img + static_cast<int64_t>(j) * C::KV_BYTES;
-        mbar_arrive_expect_tx(c.bar(C::FULL + st), C::KV_BYTES);
-#pragma unroll
-        for (int part = 0; part < 4; ++part) bulk_load(dst + part * C::HALF, src + part * C::HALF, C::HALF, c.bar(C::FULL + st));
+        if (j >= C::NS && !c.wait(empty + st, j / C::NS - 1)) break;
+        const uint8_t* src = img + static_cast<int64_t>(j) * (2 * C::SLOT);
+        mbar_arrive_expect_tx(c.bar(full + st), C::SLOT);
+        bulk_load(ring + st * C::SLOT, src, C::HALF, c.bar(full + st));
+        bulk_load(ring + st * C::SLOT + C::HALF, src + C::HALF, C::HALF, c.bar(full + st));
         ++issued;
     }
     // Every copy issued lands before the CTA's shared memory is released.
     for (int s = 0; s < C::NS && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / C::NS) * C::NS;
-        mbar_wait_drain(c.bar(C::FULL + s), (last / C::NS) & 1);
+        mbar_wait_drain(c.bar(full + s), (last / C::NS) & 1);
     }
 }
 
@@ -335,10 +364,10 @@ __device__ __forceinline__ void x3_mma(const X3Ctx& c, uint32_t s0, uint32_t tme
     // S(j) = Q_lo K_hi^T + Q_hi K_lo^T + Q_hi K_hi^T, Q from tensor memory.
     auto issue_s = [&](int j) -> bool {
         const int st = j % C::NS, sb = j & 1;
-        if (!c.wait(C::FULL + st, j / C::NS)) return false;
+        if (!c.wait(C::K_FULL + st, j / C::NS)) return false;
         if (j >= 2 && !c.wait(C::S_FREE + sb, (j >> 1) - 1)) return false;
         tc_fence_after();
-        const uint32_t kb = s0 + C::KV_OFF + st * C::KV_BYTES;
+        const uint32_t kb = s0 + C::K_OFF + st * C::SLOT;
         const uint64_t dkh = dz + (kb >> 4), dkl = dz + ((kb + C::HALF) >> 4);
         const uint32_t scol = tmem + (sb ? C::SC1 : C::SC0);
 #pragma unroll
@@ -357,15 +386,16 @@ __device__ __forceinline__ void x3_mma(const X3Ctx& c, uint32_t s0, uint32_t tme
             mma_ts_tf32(scol, tmem + C::QH + kk * 8, dkh + off, id_s, 1u);
         }
         mma_commit(c.bar(C::S_FULL + sb));
+        mma_commit(c.bar(C::K_EMPTY + st));
         return true;
     };
     // O (+)= P_lo V_hi + P_hi V_lo + P_hi V_hi, P from shared memory, V^T
     // K-major; the first product of the tile overwrites O.
     auto issue_pv = [&](int j) -> bool {
         const int st = j % C::NS;
-        if (!c.wait(C::P_FULL, j)) return false;
+        if (!c.wait(C::V_FULL + st, j / C::NS) || !c.wait(C::P_FULL, j)) return false;
         tc_fence_after();
-        const uint32_t vb = s0 + C::KV_OFF + st * C::KV_BYTES + 2 * C::HALF;
+        const uint32_t vb = s0 + C::V_OFF + st * C::SLOT;
         const uint64_t dvh = dz + (vb >> 4), dvl = dz + ((vb + C::HALF) >> 4);
         const uint64_t dph = dz + ((s0 + C::P_OFF) >> 4), dpl = dz + ((s0 + C::P_OFF + C::P_HALF) >> 4);
         const uint32_t ocol = tmem + C::OC;
@@ -376,7 +406,7 @@ __device__ __forceinline__ void x3_mma(const X3Ctx& c, uint32_t s0, uint32_t tme
 #pragma unroll
         for (int kk = 0; kk < kBN / 8; ++kk) mma_ss_tf32(ocol, dph + kk * 2, dvh + kk * 2, id_o, 1u);
         mma_commit(c.bar(C::O_DONE));
-        mma_commit(c.bar(C::EMPTY + st));
+        mma_commit(c.bar(C::V_EMPTY + st));
         return true;
     };
     bool ok = nb > 0 && c.wait(C::Q_READY, 0);
@@ -406,18 +436,22 @@ __global__ void __launch_bounds__(kThreads, 1) x3_fwd(const X3Params p) {
     c.abort = reinterpret_cast<volatile int*>(misc + 1);
     c.err = p.err;
     const int warp = threadIdx.x / 32;
-    // Heaviest query tiles (the last ones, under the causal mask) first.
+    // The query tiles of one head are adjacent, heaviest (last, under the
+    // causal mask) first: the CTAs resident at one time cover a few heads,
+    // whose K/V images stay in L2 while all their query tiles read them.
     const int mtiles = (p.M + kBM - 1) / kBM;
-    const int mt = mtiles - 1 - static_cast<int>(blockIdx.x / p.bh_count);
-    const int bh = static_cast<int>(blockIdx.x % p.bh_count);
+    const int mt = mtiles - 1 - static_cast<int>(blockIdx.x % mtiles);
+    const int bh = static_cast<int>(blockIdx.x / mtiles);
     const int r0 = mt * kBM;
     const int kend = p.causal ? min(p.N, min(p.M, r0 + kBM)) : p.N;
     const int nb = (kend + kBN - 1) / kBN;
     const int nt = (p.N + kBN - 1) / kBN;
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
-            mbar_init(c.bar(C::FULL + i), 1);
-            mbar_init(c.bar(C::EMPTY + i), 1);
+            mbar_init(c.bar(C::K_FULL + i), 1);
+            mbar_init(c.bar(C::K_EMPTY + i), 1);
+            mbar_init(c.bar(C::V_FULL + i), 1);
+            mbar_init(c.bar(C::V_EMPTY + i), 1);
         }
         mbar_init(c.bar(C::Q_READY), kBM);
         mbar_init(c.bar(C::S_FULL + 0), 1);
@@ -440,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) x3_fwd(const X3Params p) {
     const uint32_t tmem = misc[0];
     if (warp < 4) {
         x3_softmax<D>(p, c, s0, tmem, bh, r0, nb);
-    } else if (warp == 4) {
-        if ((threadIdx.x & 31) == 0) x3_producer<D>(p, c, s0, bh, nb, nt);
+    } else if (warp == 4 || warp == 6) {
+        if ((threadIdx.x & 31) == 0) x3_producer<D>(p, c, s0, bh, nb, nt, warp == 6 ? 1 : 0);
     } else if ((threadIdx.x & 31) == 0) {
         x3_mma<D>(c, s0, tmem, nb);
     }
