@@ -131,21 +131,29 @@ __global__ void __launch_bounds__(kSplitThreads) x3_split(const float* __restric
         *reinterpret_cast<float4*>(out + dst) = h;
         *reinterpret_cast<float4*>(out + HALF + dst) = l;
     }
-    // V^T: four consecutive keys of one column d per item; d runs fastest
-    // across the threads so the reads of one key row coalesce.
+    // V^T: the block's rows are staged in shared memory (coalesced float4
+    // reads), then each item takes four consecutive keys of one column d;
+    // the keys run fastest across the threads, so the eight 16-byte units of
+    // one 128-byte output row are written by neighbouring threads.
+    __shared__ float sv[kBN][D + 1];   // +1: column reads spread over the banks
+    for (int i = threadIdx.x; i < kBN * KU; i += kSplitThreads) {
+        const int r = i / KU, c = (i % KU) * 4;
+        const int key = j * kBN + r;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (key < N) x = *reinterpret_cast<const float4*>(vh + static_cast<int64_t>(key) * D + c);
+        sv[r][c + 0] = x.x;
+        sv[r][c + 1] = x.y;
+        sv[r][c + 2] = x.z;
+        sv[r][c + 3] = x.w;
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < D * (kBN / 4); i += kSplitThreads) {
-        const int d = i % D, c = (i / D) * 4;   // c: key within the block
-        float x[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int key = j * kBN + c + e;
-            x[e] = key < N ? vh[static_cast<int64_t>(key) * D + d] : 0.f;
-        }
+        const int c = (i % (kBN / 4)) * 4, d = i / (kBN / 4);   // c: key within the block
         float4 h, l;
-        split_tf32(x[0], h.x, l.x);
-        split_tf32(x[1], h.y, l.y);
-        split_tf32(x[2], h.z, l.z);
-        split_tf32(x[3], h.w, l.w);
+        split_tf32(sv[c + 0][d], h.x, l.x);
+        split_tf32(sv[c + 1][d], h.y, l.y);
+        split_tf32(sv[c + 2][d], h.z, l.z);
+        split_tf32(sv[c + 3][d], h.w, l.w);
         const int dst = (c >> 5) * (D * 32) + swz(d, c & 31);
         *reinterpret_cast<float4*>(out + 2 * HALF + dst) = h;
         *reinterpret_cast<float4*>(out + 3 * HALF + dst) = l;
