@@ -132,33 +132,37 @@ class ClockSampler:
         return summarize_clocks(rows)
 
 
-# Sources of the bf16 kernel; a recorded ncu traffic figure is reported only
-# while these hash to the value it was taken with.
+# Sources of each path's kernels; a recorded ncu traffic figure is reported
+# only while these hash to the value it was taken with.
 KERNEL_SOURCES = ["fa_bf16_kernel.cuh", "ptx.cuh", "fa_internal.h", "fa_api.cu",
                   "fa_bf16_d64.cu", "fa_bf16_d96.cu", "fa_bf16_d128.cu"]
-TRAFFIC_FILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                            "fa_fwd_bf16_dram_traffic.json")
+X3_SOURCES = ["fa_f32x3.cu", "ptx.cuh", "fa_internal.h", "fa_api.cu"]
+PROFILES = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
+TRAFFIC_FILE = os.path.join(PROFILES, "fa_fwd_bf16_dram_traffic.json")
+X3_TRAFFIC_FILE = os.path.join(PROFILES, "fa_fwd_f32x3_dram_traffic.json")
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(sources=None) -> str:
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "flashattention_fa_fwd_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes (read + written) of one launch of the bf16 kernel on this
-    workload, from the ncu capture recorded under profiles/, or None when
+def recorded_traffic(workload: str, path: str = "bf16"):
+    """DRAM bytes (read + written) of one step of a path on this workload
+    (bf16: the one kernel launch; x3: the split pre-pass plus the attention
+    kernel), from the ncu capture recorded under profiles/, or None when
     there is none or the kernel sources changed since it was taken."""
+    file, sources = (X3_TRAFFIC_FILE, X3_SOURCES) if path == "x3" else (TRAFFIC_FILE, KERNEL_SOURCES)
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(file) as f:
             rec = json.load(f)
-        if rec.get("kernel_sha") != kernel_sources_sha():
+        if rec.get("kernel_sha") != kernel_sources_sha(sources):
             return None
         e = rec["workloads"].get(workload)
         return None if e is None else int(e["dram_bytes_read"]) + int(e["dram_bytes_write"])
@@ -517,7 +521,8 @@ def gpu_arm(args, w, rank, world, local_rank):
         "pct_of_peak": 100.0 * value / world * (3.0 if x3 else 1.0) / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
-                     "traffic": recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 and not bwd else None,
+                     "traffic": (recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 and not bwd else
+                                 recorded_traffic(w.describe()["workload"], "x3") if x3 else None),
                      "peak_source": peak_source,
                      "frac_of_sustained": frac_sust,
                      "launch_ms": launch_ms},
