@@ -25,7 +25,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfa_fwd.so")
 STAMP = os.path.join(BUILD_DIR, "libfa_fwd.arch")
 
-SOURCES = ["fa_api.cu", "fa_f32.cu", "fa_f32x3.cu", "fa_bwd.cu", "fa_combine.cu", "fa_bf16_d64.cu", "fa_bf16_d96.cu",
+SOURCES = ["fa_api.cu", "fa_f32.cu", "fa_f32x3.cu", "fa_bwd.cu", "fa_bwd_tc.cu", "fa_combine.cu", "fa_bf16_d64.cu", "fa_bf16_d96.cu",
            "fa_bf16_d128.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

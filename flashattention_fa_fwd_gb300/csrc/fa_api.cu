@@ -763,7 +763,8 @@ FA_API fa_status fa_selftest_wait_timeout(int64_t limit_us, void* stream) {
 // ---------------------------------------------------------------------------
 FA_API int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t M) {
     if (B < 0 || H < 0 || M < 0) return -1;
-    return B * H * M * static_cast<int64_t>(sizeof(float));
+    const int64_t mpad = (M + 127) / 128 * 128;   // Dl and the base-2 LSE, padded to 128-row tiles
+    return 2 * B * H * mpad * static_cast<int64_t>(sizeof(float));
 }
 
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -791,8 +792,11 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
         overlaps(dq, qb, q, bh * M * D * 2) || overlaps(dk, kb, k, bh * N * D * 2) || overlaps(dv, kb, v, bh * N * D * 2) ||
         overlaps(workspace, need, dq, qb) || overlaps(workspace, need, dk, kb) || overlaps(workspace, need, dv, kb))
         return fail(FA_ERR_INVALID_ARG, "the gradients and the workspace must not overlap each other or the inputs");
+    // D in {64, 96, 128}: the tensor-core kernels (TMA maps); other D: the
+    // CUDA-core kernels.
+    const bool tc = (D == 64 || D == 96 || D == 128);
     uint32_t* word = nullptr;
-    if ((st = device_setup(false, &word)) != FA_OK) return st;
+    if ((st = device_setup(tc, &word)) != FA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (M == 0) {   // no query rows: every key gets zero gradient
@@ -807,7 +811,10 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
     p.o = static_cast<const __nv_bfloat16*>(o);
     p.dout = static_cast<const __nv_bfloat16*>(dout);
     p.lse = lse;
+    p.Mpad = static_cast<int>((M + 127) / 128 * 128);
     p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + bh * p.Mpad;
+    p.err = word;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -817,7 +824,19 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
     p.D = static_cast<int>(D);
     p.scale = scale;
     p.causal = causal != 0;
-    e = fa::launch_bwd(p, s);
+    e = fa::launch_bwd_rowdot(p, s);
+    if (e == cudaSuccess && !tc) e = fa::launch_bwd(p, s);
+    if (e == cudaSuccess && tc) {
+        CUtensorMap mq, mk, mv, mdo;
+        if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK || (st = encode_map(&mdo, dout, M, bh, D)) != FA_OK) return st;
+        if (N > 0) {
+            if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK || (st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+        } else {
+            mk = mq;  // never read: no key tiles exist
+            mv = mq;
+        }
+        e = fa::launch_bwd_tc(mq, mk, mv, mdo, p, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "launching the backward kernels");
     return FA_OK;
 }

@@ -8,7 +8,9 @@
 //   dV = P^T dO,  dP = dO V^T,  Dl_i = sum_d dO_id O_id,
 //   dS = P * (dP - Dl),  dQ = scale dS K,  dK = scale dS^T Q.
 // Three kernels, each reading bf16 inputs and accumulating in fp32:
-//   bwd_rowdot: Dl_i for every query row (one warp per row);
+//   bwd_rowdot: Dl_i for every query row (one warp per row), with the LSE in
+//               base 2, into a workspace padded to 128-row tiles (it also
+//               feeds the tensor-core kernels of fa_bwd_tc.cu);
 //   bwd_dkdv:   one CTA per 64-key tile of one head; query rows stream through
 //               shared memory in chunks; dK and dV of the tile stay in
 //               registers (eight threads per key at D = 128, four below,
@@ -58,17 +60,32 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// One warp per row of the padded [BH, Mpad] layout: Dl = sum_d dO * O and
+// the LSE in base-2 units; rows past M get Dl = 0 and LSE = +inf (P = 0).
 __global__ void bwd_rowdot(const BwdParams p) {
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    const int64_t prow = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    if (row >= static_cast<int64_t>(p.bh_count) * p.M) return;
+    if (prow >= static_cast<int64_t>(p.bh_count) * p.Mpad) return;
+    const int64_t bh = prow / p.Mpad;
+    const int r = static_cast<int>(prow - bh * p.Mpad);
+    if (r >= p.M) {
+        if (lane == 0) {
+            p.delta[prow] = 0.f;
+            p.lse2[prow] = INFINITY;
+        }
+        return;
+    }
+    const int64_t row = bh * p.M + r;
     const __nv_bfloat16* o = p.o + row * p.D;
     const __nv_bfloat16* d = p.dout + row * p.D;
     float s = 0.f;
     for (int i = lane; i < p.D; i += 32) s = fmaf(ld_bf16(o + i), ld_bf16(d + i), s);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) p.delta[row] = s;
+    if (lane == 0) {
+        p.delta[prow] = s;
+        p.lse2[prow] = p.lse[row] * kLog2e;
+    }
 }
 
 // Copies `rows` rows of width D (bf16, row-major) starting at row r0 into
@@ -115,7 +132,7 @@ __global__ void __launch_bounds__(threads<DV>()) bwd_dkdv(const BwdParams p) {
             const bool in = r0 + i < p.M;
             const int64_t row = static_cast<int64_t>(bh) * p.M + r0 + i;
             slse[i] = in ? p.lse[row] : -INFINITY;
-            sdl[i] = in ? p.delta[row] : 0.f;
+            sdl[i] = in ? p.delta[static_cast<int64_t>(bh) * p.Mpad + r0 + i] : 0.f;
         }
         __syncthreads();
         for (int i = 0; i < kChunk; ++i) {
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(threads<DV>()) bwd_dq(const BwdParams p) {
         dq[c] = 0.f;
     }
     const float lse = rvalid ? p.lse[static_cast<int64_t>(bh) * p.M + row] : -INFINITY;
-    const float dl = rvalid ? p.delta[static_cast<int64_t>(bh) * p.M + row] : 0.f;
+    const float dl = rvalid ? p.delta[static_cast<int64_t>(bh) * p.Mpad + row] : 0.f;
     const float cs = p.scale * kLog2e;
     // Keys any row of this tile can see: all, or (causal) keys <= its last row.
     const int key_hi = p.causal ? min(p.N, min(p.M, row0 + kTile)) : p.N;
@@ -222,13 +239,15 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
-    const int64_t rows = static_cast<int64_t>(p.bh_count) * p.M;
+cudaError_t launch_bwd_rowdot(const BwdParams& p, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(p.bh_count) * p.Mpad;
     const int64_t blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     bwd_rowdot<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s) {
     if (p.D <= 32) return launch_bwd_t<32>(p, s);
     if (p.D <= 64) return launch_bwd_t<64>(p, s);
     return launch_bwd_t<128>(p, s);

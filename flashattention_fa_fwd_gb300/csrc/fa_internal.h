@@ -67,7 +67,10 @@ struct BwdParams {
     const __nv_bfloat16* o;      // [BH, M, D] forward output
     const __nv_bfloat16* dout;   // [BH, M, D] gradient of the loss with respect to O
     const float* lse;            // [BH, M] forward log-sum-exp (natural log)
-    float* delta;                // [BH, M] workspace: sum_d dO * O per row
+    float* delta;                // [BH, Mpad] workspace: sum_d dO * O per row (0 past M)
+    float* lse2;                 // [BH, Mpad] workspace: lse * log2(e) (+inf past M)
+    uint32_t* err;               // device status word (tensor-core kernels' bounded waits)
+    int Mpad;                    // M rounded up to a multiple of 128
     float* dq;                   // [BH, M, D]
     float* dk;                   // [BH, N, D]
     float* dv;                   // [BH, N, D]
@@ -79,8 +82,17 @@ struct BwdParams {
     int causal;
 };
 
-// Launches the three backward kernels (row dots, dK/dV, dQ) on `s`.
+// Row dots Dl and the padded base-2 LSE (both into the workspace) on `s`.
+cudaError_t launch_bwd_rowdot(const BwdParams& p, cudaStream_t s);
+
+// The CUDA-core dK/dV and dQ kernels (after launch_bwd_rowdot) on `s`.
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t s);
+
+// The tensor-core dK/dV and dQ kernels (after launch_bwd_rowdot) on `s`, for
+// D in {64, 96, 128}; maps are fa_fwd's bf16 {D, rows, B*H} maps of Q, K, V
+// and dO.
+cudaError_t launch_bwd_tc(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& dout,
+                          const BwdParams& p, cudaStream_t s);
 
 // Arguments of the fp32 tensor-core path (three TF32 products per matrix
 // product): fp32 Q, K, V in, fp32 O and LSE out.

@@ -279,6 +279,14 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        FA_W8(0), FA_W8(8)
+        : "memory");
+}
+
 // Waits for this thread's outstanding tcgen05.ld; the register array is
 // threaded through the asm so no use of it can be scheduled before the wait.
 template <int N>

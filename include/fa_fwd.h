@@ -267,8 +267,12 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
  * of P is rebuilt as exp(S - L) from Q, K and the forward's per-row
  * log-sum-exp L (`lse`). With that P: dV = P^T dO, dP = dO V^T,
  * dS = P * (dP - rowsum(dO * O)), dQ = scale dS K, dK = scale dS^T Q.
- * This first version runs on the CUDA cores with fp32 arithmetic (bf16
- * inputs read exactly) and is deterministic (no atomics).
+ * D in {64, 96, 128} runs on the tensor cores (tcgen05, TMA): one kernel
+ * per 128-key tile computes S^T = K Q^T and dP^T = V dO^T, rebuilds P^T and
+ * dS^T (bf16) in tensor memory and accumulates dV, dK there; one per
+ * 128-row query tile does the same for dQ. Other D run on the CUDA cores in
+ * fp32. Both are deterministic (each output written by one CTA, no
+ * atomics).
  *
  *   q, k, v          the forward's bf16 inputs, [B,H,M,D] / [B,H,N,D]
  *   o, lse           the forward's outputs for them (bf16 O, fp32 LSE)
@@ -290,7 +294,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,
                  float scale, int causal, void* workspace, int64_t workspace_bytes, void* stream);
 
-/* Workspace bytes fa_bwd needs: B*H*M fp32 values (-1 for negative sizes).
+/* Workspace bytes fa_bwd needs: two fp32 values per (head, query row) with
+ * the rows padded to a multiple of 128 (-1 for negative sizes).
  * Needs no GPU. */
 int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t M);
 

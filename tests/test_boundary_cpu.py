@@ -154,7 +154,7 @@ def test_wait_selftest_rejects_bad_limits(lib):
 
 
 def test_bwd_workspace_size_and_checks(lib):
-    assert fa.fa_bwd_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 4
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100) == 2 * 2 * 3 * 128 * 4   # Dl and base-2 LSE, rows padded to 128
     assert fa.fa_bwd_workspace_bytes(-1, 3, 100) == -1
     W = 64 * A
     grads = (6 * A, 7 * A, 8 * A)
