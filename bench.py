@@ -495,6 +495,11 @@ def gpu_arm(args, w, rank, world, local_rank):
         peak_source = (f"{peaks.get('source')} bf16_tflops x 1.1/2.25 (nominal dense TF32 : BF16); achieved "
                        f"counts the 3 TF32 products per attention FLOP")
         frac_sust = achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * 1.1 / 2.25)
+    elif bwd and w.D in (64, 96, 128):
+        # The tensor-core backward: achieved counts the algorithm's five products (its
+        # kernels execute seven: S and dP are rebuilt in both the dK/dV and the dQ kernel).
+        peak_source = (f"{peaks.get('source')} bf16_tflops (burst); achieved counts the 5 products of the "
+                       f"recomputing backward (7 executed)")
     elif not bf16 or bwd:
         # The fp32 path and the backward run on the CUDA cores (fp32 FMA, no tensor cores):
         # its ceiling is SMs x 128 fp32 lanes x 2 FLOP per FMA x max SM clock.

@@ -343,7 +343,11 @@ def _check_grad(g, ref, what):
 
 @pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 200, 300, 64, False), (2, 1, 257, 129, 128, True),
                                               (1, 3, 100, 100, 96, True), (1, 1, 1, 7, 64, False),
-                                              (1, 2, 190, 70, 32, True), (1, 1, 64, 64, 17, False)])
+                                              (1, 2, 190, 70, 32, True), (1, 1, 64, 64, 17, False),
+                                              (1, 2, 600, 600, 128, True), (2, 2, 300, 700, 64, False),
+                                              (1, 1, 700, 300, 96, True), (1, 2, 384, 384, 64, True),
+                                              (1, 1, 129, 1, 128, False), (1, 1, 130, 260, 128, False),
+                                              (1, 1, 100, 300, 64, True)])
 def test_bwd_matches_oracle(B, H, M, N, D, causal):
     import torch
 
@@ -376,6 +380,39 @@ def test_bwd_matches_oracle(B, H, M, N, D, causal):
     ref = attention_bwd(q, k, v, do, scale, causal)
     for name, g, r in zip(("dq", "dk", "dv"), grads[0], ref):
         _check_grad(g.cpu().numpy(), r, f"{name} B{B} H{H} M{M} N{N} D{D} causal={causal}")
+
+
+@pytest.mark.parametrize("name,heads", [("causal_b8_h32_s4096_d128", (0, 255)),
+                                        ("gpt2m_b64_h16_s1024_d64", (0, 517, 1023))])
+def test_bwd_full_size_sampled_heads(name, heads):
+    """The backward on a whole benchmark workload (the bench's launch shape),
+    checked head by head against the oracle on sampled heads; every gradient
+    finite."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    do = round_to_bf16(np.random.default_rng(4242).standard_normal(q.shape, dtype=np.float32))
+    tq, tk, tv, tdo = (torch.from_numpy(x).cuda().to(torch.bfloat16) for x in (q, k, v, do))
+    o = torch.empty_like(tq)
+    lse = torch.empty(w.B, w.H, w.M, device="cuda")
+    fa.fa_fwd(tq, tk, tv, o, lse, w.scale, w.causal)
+    dq = torch.empty(tq.shape, device="cuda")
+    dk = torch.empty(tk.shape, device="cuda")
+    dv = torch.empty(tv.shape, device="cuda")
+    fa.fa_bwd(tq, tk, tv, o, lse, tdo, dq, dk, dv, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for g in (dq, dk, dv):
+        assert bool(torch.isfinite(g).all())
+    flat = lambda x: x.reshape(w.B * w.H, *x.shape[2:])
+    for h in heads:
+        b, hh = divmod(h, w.H)
+        ref = attention_bwd(q[b, hh], k[b, hh], v[b, hh], do[b, hh], w.scale, w.causal)
+        for gname, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            _check_grad(flat(g)[h].cpu().numpy(), r, f"{name} head {h} {gname}")
 
 
 # ------------------------------------------------ full-size workloads (sampled)
