@@ -79,7 +79,18 @@ __global__ void bwd_rowdot(const BwdParams p) {
     const __nv_bfloat16* o = p.o + row * p.D;
     const __nv_bfloat16* d = p.dout + row * p.D;
     float s = 0.f;
-    for (int i = lane; i < p.D; i += 32) s = fmaf(ld_bf16(o + i), ld_bf16(d + i), s);
+    if ((p.D & 3) == 0) {   // rows 8-byte aligned: four bf16 per lane and load
+        for (int i = lane * 4; i < p.D; i += 128) {
+            const uint2 ov = *reinterpret_cast<const uint2*>(o + i), dv = *reinterpret_cast<const uint2*>(d + i);
+            const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov.x));
+            const float2 o1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov.y));
+            const float2 d0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.x));
+            const float2 d1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dv.y));
+            s = fmaf(o0.x, d0.x, fmaf(o0.y, d0.y, fmaf(o1.x, d1.x, fmaf(o1.y, d1.y, s))));
+        }
+    } else {
+        for (int i = lane; i < p.D; i += 32) s = fmaf(ld_bf16(o + i), ld_bf16(d + i), s);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) {

@@ -36,7 +36,10 @@ namespace fa {
 namespace {
 
 constexpr int kT = 128;            // rows of every tile (queries or keys)
-constexpr int kThreads = 192;      // 4 softmax/epilogue warps, the TMA warp, the MMA warp
+// Warps 0-7: two warpgroups that rebuild P and dS (each over half of a
+// buffer's 64 columns) and write the results; warp 8: TMA; warp 9: MMA.
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -52,15 +55,21 @@ struct BwdCfg {
     static constexpr int FIX_OFF = 0;                    // the CTA's resident pair (K and V, or Q and dO)
     static constexpr int RING_OFF = 2 * TILE;
     static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE;
-    static constexpr int FIX_FULL = 0, FULL = 1, EMPTY = 1 + STAGES, S_FULL = 1 + 2 * STAGES;
-    static constexpr int P_FULL = S_FULL + 1, DONE = P_FULL + 1, DRAIN = DONE + 1, NUM_BARS = DRAIN + 1;
+    static constexpr int FIX_FULL = 0, FULL = 1, EMPTY = 1 + STAGES, S_FULL = 1 + 2 * STAGES;   // S_FULL, P_FULL: one per S buffer
+    static constexpr int P_FULL = S_FULL + 2, S_READ = P_FULL + 2, DONE = S_READ + 2, DRAIN = DONE + 1;
+    static constexpr int NUM_BARS = DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
-    // Tensor memory: S (then P, bf16 pairs in its first 64 columns), dP
-    // (then dS), then the accumulators (dV and dK, or dQ).
+    // Every 128-row streamed tile is handled as two 64-row halves, each with
+    // its own S and dP buffer, so that one half's rebuild of P and dS runs
+    // while the other half's products are computed. Tensor memory: S buffers
+    // (then P, bf16 pairs in their first 32 columns) at 0 and 64, dP buffers
+    // (then dS) at 128 and 192, then the accumulators (dV and dK, or dQ).
+    static constexpr int HALF_ROWS = 64;
+    static constexpr int HALF_BYTES = HALF_ROWS * 128;   // a half's row offset inside every panel
     static constexpr uint32_t TS = 0, TDP = 128, TACC = 256;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, false);   // 128 x 128, both K-major
+    static constexpr uint32_t ID_SS = idesc_bf16_f32(128, HALF_ROWS, false);  // 128 x 64, both K-major
     static constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, true);     // 128 x D, B MN-major
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(TACC + 2 * D <= TMEM_COLS, "tensor memory");
@@ -99,7 +108,8 @@ __device__ __forceinline__ uint32_t kstep(int kk) {
     return (kk >> 2) * (BwdCfg<D>::PANEL >> 4) + (kk & 3) * 2;
 }
 
-// D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major tiles in shared memory.
+// D[128 x 64] = A[128 x D] B[64 x D]^T, both K-major in shared memory (B:
+// half a tile, `b` already offset to its first row).
 template <int D>
 __device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a, uint32_t b) {
     const uint64_t da = desc_kmajor(a), db = desc_kmajor(b);
@@ -108,22 +118,23 @@ __device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a, uint32_
         mma_ss(d_tmem, da + kstep<D>(kk), db + kstep<D>(kk), BwdCfg<D>::ID_SS, kk > 0 ? 1u : 0u);
 }
 
-// Acc[128 x D] (+)= A[128 x 128] (bf16 pairs in tensor memory) B[128 x D]
-// (a tile in shared memory read MN-major: its rows are the K dimension).
+// Acc[128 x D] (+)= A[128 x 64] (bf16 pairs in tensor memory) B[64 x D]
+// (half a tile in shared memory read MN-major: its rows are the K dimension).
 template <int D>
 __device__ __forceinline__ void mma_tile_acc(uint32_t acc, uint32_t a_tmem, uint32_t b, bool first) {
     const uint64_t db = desc_mnmajor<D>(b);
 #pragma unroll
-    for (int kk = 0; kk < kT / 16; ++kk)
+    for (int kk = 0; kk < BwdCfg<D>::HALF_ROWS / 16; ++kk)
         mma_ts(acc, a_tmem + kk * 8, db + kk * (2048 >> 4), BwdCfg<D>::ID_ACC, (first && kk == 0) ? 0u : 1u);
 }
 
 // This thread's row of a 128 x D fp32 accumulator (its tensor-memory lane),
 // times `mul`, to global memory; zeros when `have` is false.
 template <int D>
-__device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool in, float* dst, float mul) {
+__device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool in, float* dst, float mul,
+                                              int cc_lo = 0, int cc_hi = D / 32) {
 #pragma unroll 1
-    for (int cc = 0; cc < D / 32; ++cc) {
+    for (int cc = cc_lo; cc < cc_hi; ++cc) {
         uint32_t r[32];
         if (have) {
             tmem_ld_x32(tm_acc + cc * 32, r);
@@ -146,24 +157,74 @@ __device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool i
 }
 
 // Rebuilds 32 columns of this thread's row of P and dS from S and dP in
-// tensor memory: p = exp2(s * cs - L2), zero outside [lo, hi); ds = p (dp - Dl).
-// L2 and Dl are per column (dK/dV kernel) or per row (dQ kernel).
-template <bool PER_COLUMN>
+// tensor memory: p = exp2(s * cs - L2), zero outside columns [lo, hi) of the
+// chunk when MASK; ds = p (dp - Dl). L2 and Dl are per column (dK/dV kernel,
+// `l2` and `dl` pointing at the chunk's first column, 16-byte aligned) or
+// per row (dQ kernel).
+template <bool PER_COLUMN, bool MASK>
 __device__ __forceinline__ void rebuild_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float cs,
-                                              const float* l2, const float* dl, float l2_row, float dl_row,
-                                              int c_base, int lo, int hi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+                                              const float* l2, const float* dl, float l2_row, float dl_row, int lo,
+                                              int hi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int c0 = c_base + 2 * i;
-        const float la = PER_COLUMN ? l2[c0] : l2_row, lb = PER_COLUMN ? l2[c0 + 1] : l2_row;
-        const float da = PER_COLUMN ? dl[c0] : dl_row, db = PER_COLUMN ? dl[c0 + 1] : dl_row;
-        float pa = ex2(fmaf(__uint_as_float(sr[2 * i]), cs, -la));
-        float pb = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), cs, -lb));
-        pa = (c0 >= lo && c0 < hi) ? pa : 0.f;
-        pb = (c0 + 1 >= lo && c0 + 1 < hi) ? pb : 0.f;
-        pp[i] = pack_bf16x2(pa, pb);
-        dd[i] = pack_bf16x2(pa * (__uint_as_float(dr[2 * i]) - da), pb * (__uint_as_float(dr[2 * i + 1]) - db));
+    for (int i = 0; i < 8; ++i) {
+        float lv[4], dv[4];
+        if (PER_COLUMN) {
+            const float4 a = *reinterpret_cast<const float4*>(l2 + 4 * i);
+            const float4 b = *reinterpret_cast<const float4*>(dl + 4 * i);
+            lv[0] = a.x, lv[1] = a.y, lv[2] = a.z, lv[3] = a.w;
+            dv[0] = b.x, dv[1] = b.y, dv[2] = b.z, dv[3] = b.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) lv[e] = l2_row, dv[e] = dl_row;
+        }
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = 4 * i + e;
+            pv[e] = ex2(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
+            if (MASK) pv[e] = (c >= lo && c < hi) ? pv[e] : 0.f;
+        }
+        pp[2 * i] = pack_bf16x2(pv[0], pv[1]);
+        pp[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
+        dd[2 * i] = pack_bf16x2(pv[0] * (__uint_as_float(dr[4 * i]) - dv[0]), pv[1] * (__uint_as_float(dr[4 * i + 1]) - dv[1]));
+        dd[2 * i + 1] =
+            pack_bf16x2(pv[2] * (__uint_as_float(dr[4 * i + 2]) - dv[2]), pv[3] * (__uint_as_float(dr[4 * i + 3]) - dv[3]));
     }
+}
+
+// One warpgroup's share of a buffer: loads its 32 columns of S and dP,
+// rebuilds P and dS and writes the bf16 pairs over columns [16 wg, 16 wg +
+// 16) of the same buffers. Warpgroup 1 writes over columns warpgroup 0 reads,
+// so it first waits for S_READ, which warpgroup 0 signals once its loads
+// are done. Returns false if a wait gave up.
+template <int D, bool PER_COLUMN, bool WRITE_P>
+__device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int b, int phase, uint32_t ts, uint32_t tdp,
+                                              float cs, const float* l2, const float* dl, float l2_row, float dl_row,
+                                              int lo, int hi) {
+    using C = BwdCfg<D>;
+    uint32_t sr[32], dr[32], pp[16], dd[16];
+    tmem_ld_x32(ts + 32 * wg, sr);
+    tmem_ld_x32(tdp + 32 * wg, dr);
+    tmem_ld_wait(sr);
+    tmem_ld_wait(dr);
+    if (wg == 0) {
+        tc_fence_before();
+        mbar_arrive(c.bar(C::S_READ + b));
+    }
+    if (lo <= 0 && hi >= 32)
+        rebuild_chunk<PER_COLUMN, false>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
+    else
+        rebuild_chunk<PER_COLUMN, true>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
+    if (wg == 1) {
+        if (!c.wait_warp(C::S_READ + b, phase)) return false;
+        tc_fence_after();
+    }
+    if (WRITE_P) tmem_st_x16(ts + 16 * wg, pp);
+    tmem_st_x16((WRITE_P ? tdp : ts) + 16 * wg, dd);
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(c.bar(C::P_FULL + b));
+    return true;
 }
 
 // Shared prologue: barriers, tensor memory.
@@ -176,14 +237,17 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
             mbar_init(c.bar(C::FULL + s), 1);
             mbar_init(c.bar(C::EMPTY + s), 1);
         }
-        mbar_init(c.bar(C::S_FULL), 1);
-        mbar_init(c.bar(C::P_FULL), kT);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(c.bar(C::S_FULL + b), 1);
+            mbar_init(c.bar(C::P_FULL + b), 2 * kT);
+            mbar_init(c.bar(C::S_READ + b), kT);
+        }
         mbar_init(c.bar(C::DONE), 1);
         mbar_init(c.bar(C::DRAIN), 1);
         misc[1] = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x / 32 == 5) {
+    if (threadIdx.x / 32 == kMmaWarp) {
         tmem_alloc(smem_u32(misc), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -197,7 +261,7 @@ template <int D>
 __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x / 32 == 5) {
+    if (threadIdx.x / 32 == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, BwdCfg<D>::TMEM_COLS);
     }
@@ -261,85 +325,89 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int i0 = p.causal ? key0 / kT : 0;
     const int nq = mtiles > i0 ? mtiles - i0 : 0;
     const uint32_t tmem = bwd_setup<D>(c, misc);
-    if (warp < 4) {
-        // Thread t owns key key0 + t (tensor-memory lane t) and rebuilds
-        // its rows of P^T and dS^T over each streamed query tile.
-        const int t = threadIdx.x;
+    if (warp < 8) {
+        // Thread t of warpgroup wg owns key key0 + t (tensor-memory lane t)
+        // and columns [32 wg, 32 wg + 32) of every 64-query half.
+        const int wg = warp >> 2, t = threadIdx.x & 127;
         const int key = key0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const float cs = p.scale * kLog2e;
         bool ok = true;
 #pragma unroll 1
-        for (int k = 0; k < nq && ok; ++k) {
+        for (int g = 0; g < 2 * nq && ok; ++g) {
+            const int k = g >> 1, h = g & 1, b = g & 1;   // query tile, half, S/dP buffer
             const int s = k % C::STAGES;
-            const int q0 = (i0 + k) * kT;
+            const int q0 = (i0 + k) * kT + h * C::HALF_ROWS + 32 * wg;   // this share's first query
             // The stage's LSE2 / Dl arrived with its tiles (FULL), which the
             // MMA thread waited for before S_FULL; wait here too so that the
             // copies are visible to this thread.
-            if (!c.wait_warp(C::FULL + s, k / C::STAGES) || !c.wait_warp(C::S_FULL, k)) {
+            if (!c.wait_warp(C::FULL + s, k / C::STAGES) || !c.wait_warp(C::S_FULL + b, g >> 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE);
+            const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) +
+                              h * C::HALF_ROWS + 32 * wg;
             const float* dl = l2 + kT;
             // Visible queries: column c with q0 + c >= key (causal); rows past
             // M have L2 = +inf; a key past N sees nothing.
             const int lo = p.causal ? key - q0 : 0;
-            const int hi = key < p.N ? kT : 0;
-#pragma unroll 1
-            for (int cc = 0; cc < kT / 32; ++cc) {
-                uint32_t sr[32], dr[32], pp[16], dd[16];
-                tmem_ld_x32(tm + C::TS + cc * 32, sr);
-                tmem_ld_x32(tm + C::TDP + cc * 32, dr);
-                tmem_ld_wait(sr);
-                tmem_ld_wait(dr);
-                rebuild_chunk<true>(sr, dr, cs, l2, dl, 0.f, 0.f, cc * 32, lo, hi, pp, dd);
-                // Column pair 2i of this chunk lands in column cc * 16 + i,
-                // inside the chunks already read.
-                tmem_st_x16(tm + C::TS + cc * 16, pp);
-                tmem_st_x16(tm + C::TDP + cc * 16, dd);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(c.bar(C::P_FULL));
+            const int hi = key < p.N ? 32 : 0;
+            ok = rebuild_share<D, true, true>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs, l2, dl,
+                                              0.f, 0.f, lo, hi);
         }
         if (ok && nq > 0) {
             ok = c.wait_warp(C::DONE, 0);
             tc_fence_after();
         }
-        if (ok) {
+        if (ok) {   // warpgroup 0 writes dV, warpgroup 1 dK
             const bool in = key < p.N;
             const int64_t off = (static_cast<int64_t>(bh) * p.N + key) * D;
-            store_acc_row<D>(tm + C::TACC, nq > 0, in, p.dv + off, 1.f);
-            store_acc_row<D>(tm + C::TACC + D, nq > 0, in, p.dk + off, p.scale);
+            if (wg == 0)
+                store_acc_row<D>(tm + C::TACC, nq > 0, in, p.dv + off, 1.f);
+            else
+                store_acc_row<D>(tm + C::TACC + D, nq > 0, in, p.dk + off, p.scale);
         }
-    } else if (warp == 4) {
+    } else if (warp == kTmaWarp) {
         if ((threadIdx.x & 31) == 0 && nq > 0)
             bwd_producer<D>(c, s0, &map_k, &map_v, key0, &map_q, &map_do, i0 * kT, nq, bh, p.lse2, p.delta,
                             static_cast<int64_t>(bh) * p.Mpad + i0 * kT);
     } else if ((threadIdx.x & 31) == 0) {
-        // MMA thread. Per query tile: S^T = K Q^T and dP^T = V dO^T; once
-        // the softmax threads have turned them into P^T and dS^T (bf16, in
-        // place): dV += P^T dO, dK += dS^T Q. The next S^T overwrites P^T
-        // only after those products (one thread's MMAs run in order).
+        // MMA thread. Per half query tile g: S^T = K Q^T and dP^T = V dO^T
+        // into buffer g & 1; once the softmax threads have turned them into
+        // P^T and dS^T (bf16, in place): dV += P^T dO, dK += dS^T Q. Half
+        // g + 1's products are issued before half g's gradient products, so
+        // its rebuild overlaps them; a buffer is rewritten (half g + 2) only
+        // after half g's gradient products, which read it (one thread's MMAs
+        // run in order).
         bool ok = nq > 0 && c.wait(C::FIX_FULL, 0);
         const uint32_t kt = s0 + C::FIX_OFF, vt = kt + C::TILE;
+        auto issue_sdp = [&](int g) -> bool {
+            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
+            if (h == 0 && !c.wait(C::FULL + s, k / C::STAGES)) return false;
+            tc_fence_after();
+            const uint32_t qt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, dot = qt + C::TILE;
+            mma_tile_nt<D>(tmem + C::TS + (g & 1) * 64, kt, qt);
+            mma_tile_nt<D>(tmem + C::TDP + (g & 1) * 64, vt, dot);
+            mma_commit(c.bar(C::S_FULL + (g & 1)));
+            return true;
+        };
+        auto issue_grad = [&](int g) -> bool {
+            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
+            if (!c.wait(C::P_FULL + (g & 1), g >> 1)) return false;
+            tc_fence_after();
+            const uint32_t qt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, dot = qt + C::TILE;
+            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS + (g & 1) * 64, dot, g == 0);
+            mma_tile_acc<D>(tmem + C::TACC + D, tmem + C::TDP + (g & 1) * 64, qt, g == 0);
+            if (h == 1) mma_commit(c.bar(C::EMPTY + s));
+            if (g == 2 * nq - 1) mma_commit(c.bar(C::DONE));
+            return true;
+        };
+        if (ok) ok = issue_sdp(0);
 #pragma unroll 1
-        for (int k = 0; ok && k < nq; ++k) {
-            const int s = k % C::STAGES;
-            if (!c.wait(C::FULL + s, k / C::STAGES)) break;
-            tc_fence_after();
-            const uint32_t qt = s0 + C::RING_OFF + s * C::STAGE, dot = qt + C::TILE;
-            mma_tile_nt<D>(tmem + C::TS, kt, qt);
-            mma_tile_nt<D>(tmem + C::TDP, vt, dot);
-            mma_commit(c.bar(C::S_FULL));
-            if (!c.wait(C::P_FULL, k)) break;
-            tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
-            mma_tile_acc<D>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
-            mma_commit(c.bar(C::EMPTY + s));
-            if (k == nq - 1) mma_commit(c.bar(C::DONE));
+        for (int g = 0; ok && g < 2 * nq; ++g) {
+            if (g + 1 < 2 * nq && !issue_sdp(g + 1)) break;
+            ok = issue_grad(g);
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
@@ -370,9 +438,10 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     const int kend = p.causal ? min(p.N, min(p.M, r0 + kT)) : p.N;
     const int nk = (kend + kT - 1) / kT;
     const uint32_t tmem = bwd_setup<D>(c, misc);
-    if (warp < 4) {
-        // Thread t owns query row r0 + t (tensor-memory lane t).
-        const int t = threadIdx.x;
+    if (warp < 8) {
+        // Thread t of warpgroup wg owns query row r0 + t (tensor-memory lane
+        // t) and columns [32 wg, 32 wg + 32) of every 64-key half.
+        const int wg = warp >> 2, t = threadIdx.x & 127;
         const int row = r0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const float cs = p.scale * kLog2e;
@@ -381,56 +450,58 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         const int lim = p.causal ? min(p.N, row + 1) : p.N;   // keys [0, lim) visible
         bool ok = true;
 #pragma unroll 1
-        for (int k = 0; k < nk && ok; ++k) {
-            if (!c.wait_warp(C::S_FULL, k)) {
+        for (int g = 0; g < 2 * nk && ok; ++g) {
+            const int b = g & 1;
+            if (!c.wait_warp(C::S_FULL + b, g >> 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int hi = lim - k * kT;
-#pragma unroll 1
-            for (int cc = 0; cc < kT / 32; ++cc) {
-                uint32_t sr[32], dr[32], pp[16], dd[16];
-                tmem_ld_x32(tm + C::TS + cc * 32, sr);
-                tmem_ld_x32(tm + C::TDP + cc * 32, dr);
-                tmem_ld_wait(sr);
-                tmem_ld_wait(dr);
-                rebuild_chunk<false>(sr, dr, cs, nullptr, nullptr, l2, dl, cc * 32, 0, hi, pp, dd);
-                tmem_st_x16(tm + C::TS + cc * 16, dd);   // dS pairs over S's first 64 columns
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(c.bar(C::P_FULL));
+            const int hi = lim - (g * C::HALF_ROWS + 32 * wg);   // this share's keys: g * 64 + 32 wg + column
+            ok = rebuild_share<D, false, false>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs,
+                                                nullptr, nullptr, l2, dl, 0, hi);
         }
         if (ok && nk > 0) {
             ok = c.wait_warp(C::DONE, 0);
             tc_fence_after();
         }
-        if (ok)
-            store_acc_row<D>(tm + C::TACC, nk > 0, row < p.M,
-                             p.dq + (static_cast<int64_t>(bh) * p.M + row) * D, p.scale);
-    } else if (warp == 4) {
+        if (ok)   // each warpgroup writes half of the row's 32-column chunks
+            store_acc_row<D>(tm + C::TACC, nk > 0, row < p.M, p.dq + (static_cast<int64_t>(bh) * p.M + row) * D,
+                             p.scale, wg == 0 ? 0 : (D / 32 + 1) / 2, wg == 0 ? (D / 32 + 1) / 2 : D / 32);
+    } else if (warp == kTmaWarp) {
         if ((threadIdx.x & 31) == 0 && nk > 0)
             bwd_producer<D>(c, s0, &map_q, &map_do, r0, &map_k, &map_v, 0, nk, bh, nullptr, nullptr, 0);
     } else if ((threadIdx.x & 31) == 0) {
-        // MMA thread. Per key tile: S = Q K^T and dP = dO V^T; once the
-        // softmax threads have written dS (bf16, over S): dQ += dS K.
+        // MMA thread. Per half key tile g: S = Q K^T and dP = dO V^T into
+        // buffer g & 1; once the softmax threads have written dS (bf16, over
+        // S): dQ += dS K. Issue order as in the dK/dV kernel.
         bool ok = nk > 0 && c.wait(C::FIX_FULL, 0);
         const uint32_t qt = s0 + C::FIX_OFF, dot = qt + C::TILE;
+        auto issue_sdp = [&](int g) -> bool {
+            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
+            if (h == 0 && !c.wait(C::FULL + s, k / C::STAGES)) return false;
+            tc_fence_after();
+            const uint32_t kt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, vt = kt + C::TILE;
+            mma_tile_nt<D>(tmem + C::TS + (g & 1) * 64, qt, kt);
+            mma_tile_nt<D>(tmem + C::TDP + (g & 1) * 64, dot, vt);
+            mma_commit(c.bar(C::S_FULL + (g & 1)));
+            return true;
+        };
+        auto issue_grad = [&](int g) -> bool {
+            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
+            if (!c.wait(C::P_FULL + (g & 1), g >> 1)) return false;
+            tc_fence_after();
+            const uint32_t kt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES;
+            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS + (g & 1) * 64, kt, g == 0);
+            if (h == 1) mma_commit(c.bar(C::EMPTY + s));
+            if (g == 2 * nk - 1) mma_commit(c.bar(C::DONE));
+            return true;
+        };
+        if (ok) ok = issue_sdp(0);
 #pragma unroll 1
-        for (int k = 0; ok && k < nk; ++k) {
-            const int s = k % C::STAGES;
-            if (!c.wait(C::FULL + s, k / C::STAGES)) break;
-            tc_fence_after();
-            const uint32_t kt = s0 + C::RING_OFF + s * C::STAGE, vt = kt + C::TILE;
-            mma_tile_nt<D>(tmem + C::TS, qt, kt);
-            mma_tile_nt<D>(tmem + C::TDP, dot, vt);
-            mma_commit(c.bar(C::S_FULL));
-            if (!c.wait(C::P_FULL, k)) break;
-            tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS, kt, k == 0);
-            mma_commit(c.bar(C::EMPTY + s));
-            if (k == nk - 1) mma_commit(c.bar(C::DONE));
+        for (int g = 0; ok && g < 2 * nk; ++g) {
+            if (g + 1 < 2 * nk && !issue_sdp(g + 1)) break;
+            ok = issue_grad(g);
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
