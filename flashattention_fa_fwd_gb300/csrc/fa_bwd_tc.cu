@@ -36,14 +36,18 @@ namespace fa {
 namespace {
 
 constexpr int kT = 128;            // rows of every tile (queries or keys)
-// Warps 0-7: two warpgroups that rebuild P and dS (each over half of a
-// buffer's 64 columns) and write the results; warp 8: TMA; warp 9: MMA.
-constexpr int kThreads = 320;
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
+    // Warps [0, 4 NWG): NWG warpgroups that rebuild P and dS, each over W of
+    // a buffer's 64 columns, and write the results; then the TMA warp and the
+    // MMA warp. (Four warpgroups of 16 columns measured slower than two of 32
+    // at D = 64 as well as at D = 128.)
+    static constexpr int NWG = 2;
+    static constexpr int W = 64 / NWG;
+    static constexpr int TMA_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1;
+    static constexpr int THREADS = 32 * (4 * NWG + 2);
     static constexpr int PANELS = (D + 63) / 64;         // 64-column TMA boxes per tile row
     static constexpr int PANEL = kT * 128;               // 128 rows x 128 B
     static constexpr int TILE = PANELS * PANEL;
@@ -156,17 +160,43 @@ __device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool i
     }
 }
 
-// Rebuilds 32 columns of this thread's row of P and dS from S and dP in
+// Tensor-memory loads of 16 and stores of 8 consecutive columns (32 lanes x
+// 32-bit pattern), for the narrower rebuild shares.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
+    if constexpr (W == 32) tmem_ld_x32(taddr, r);
+    else tmem_ld16(taddr, r);
+}
+template <int W>
+__device__ __forceinline__ void tmem_st_pairs(uint32_t taddr, const uint32_t (&r)[W / 2]) {
+    if constexpr (W == 32) tmem_st_x16(taddr, r);
+    else tmem_st8(taddr, r);
+}
+
+// Rebuilds W columns of this thread's row of P and dS from S and dP in
 // tensor memory: p = exp2(s * cs - L2), zero outside columns [lo, hi) of the
-// chunk when MASK; ds = p (dp - Dl). L2 and Dl are per column (dK/dV kernel,
-// `l2` and `dl` pointing at the chunk's first column, 16-byte aligned) or
+// share when MASK; ds = p (dp - Dl). L2 and Dl are per column (dK/dV kernel,
+// `l2` and `dl` pointing at the share's first column, 16-byte aligned) or
 // per row (dQ kernel).
-template <bool PER_COLUMN, bool MASK>
-__device__ __forceinline__ void rebuild_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], float cs,
+template <int W, bool PER_COLUMN, bool MASK>
+__device__ __forceinline__ void rebuild_chunk(const uint32_t (&sr)[W], const uint32_t (&dr)[W], float cs,
                                               const float* l2, const float* dl, float l2_row, float dl_row, int lo,
-                                              int hi, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
+                                              int hi, uint32_t (&pp)[W / 2], uint32_t (&dd)[W / 2]) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < W / 4; ++i) {
         float lv[4], dv[4];
         if (PER_COLUMN) {
             const float4 a = *reinterpret_cast<const float4*>(l2 + 4 * i);
@@ -192,35 +222,35 @@ __device__ __forceinline__ void rebuild_chunk(const uint32_t (&sr)[32], const ui
     }
 }
 
-// One warpgroup's share of a buffer: loads its 32 columns of S and dP,
-// rebuilds P and dS and writes the bf16 pairs over columns [16 wg, 16 wg +
-// 16) of the same buffers. Warpgroup 1 writes over columns warpgroup 0 reads,
-// so it first waits for S_READ, which warpgroup 0 signals once its loads
-// are done. Returns false if a wait gave up.
+// One warpgroup's share of a buffer: loads its W columns of S and dP,
+// rebuilds P and dS and writes the bf16 pairs over columns [W/2 wg, W/2 (wg
+// + 1)) of the same buffers. Those columns were read by a lower warpgroup,
+// so every warpgroup signals S_READ once its loads are done and all but the
+// first wait for it before writing (the first writes inside its own
+// columns). Returns false if a wait gave up.
 template <int D, bool PER_COLUMN, bool WRITE_P>
 __device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int b, int phase, uint32_t ts, uint32_t tdp,
                                               float cs, const float* l2, const float* dl, float l2_row, float dl_row,
                                               int lo, int hi) {
     using C = BwdCfg<D>;
-    uint32_t sr[32], dr[32], pp[16], dd[16];
-    tmem_ld_x32(ts + 32 * wg, sr);
-    tmem_ld_x32(tdp + 32 * wg, dr);
+    constexpr int W = C::W;
+    uint32_t sr[W], dr[W], pp[W / 2], dd[W / 2];
+    tmem_ld_cols<W>(ts + W * wg, sr);
+    tmem_ld_cols<W>(tdp + W * wg, dr);
     tmem_ld_wait(sr);
     tmem_ld_wait(dr);
-    if (wg == 0) {
-        tc_fence_before();
-        mbar_arrive(c.bar(C::S_READ + b));
-    }
-    if (lo <= 0 && hi >= 32)
-        rebuild_chunk<PER_COLUMN, false>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
+    tc_fence_before();
+    mbar_arrive(c.bar(C::S_READ + b));
+    if (lo <= 0 && hi >= W)
+        rebuild_chunk<W, PER_COLUMN, false>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
     else
-        rebuild_chunk<PER_COLUMN, true>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
-    if (wg == 1) {
+        rebuild_chunk<W, PER_COLUMN, true>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
+    if (wg > 0) {
         if (!c.wait_warp(C::S_READ + b, phase)) return false;
         tc_fence_after();
     }
-    if (WRITE_P) tmem_st_x16(ts + 16 * wg, pp);
-    tmem_st_x16((WRITE_P ? tdp : ts) + 16 * wg, dd);
+    if (WRITE_P) tmem_st_pairs<W>(ts + (W / 2) * wg, pp);
+    tmem_st_pairs<W>((WRITE_P ? tdp : ts) + (W / 2) * wg, dd);
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(c.bar(C::P_FULL + b));
@@ -239,15 +269,15 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(c.bar(C::S_FULL + b), 1);
-            mbar_init(c.bar(C::P_FULL + b), 2 * kT);
-            mbar_init(c.bar(C::S_READ + b), kT);
+            mbar_init(c.bar(C::P_FULL + b), C::NWG * kT);
+            mbar_init(c.bar(C::S_READ + b), C::NWG * kT);
         }
         mbar_init(c.bar(C::DONE), 1);
         mbar_init(c.bar(C::DRAIN), 1);
         misc[1] = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x / 32 == kMmaWarp) {
+    if (threadIdx.x / 32 == C::MMA_WARP) {
         tmem_alloc(smem_u32(misc), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -261,7 +291,7 @@ template <int D>
 __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x / 32 == kMmaWarp) {
+    if (threadIdx.x / 32 == BwdCfg<D>::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, BwdCfg<D>::TMEM_COLS);
     }
@@ -303,7 +333,7 @@ __device__ __forceinline__ void bwd_producer(const BwdCtx& c, uint32_t s0, const
 
 // ------------------------------------------------------------ dK, dV kernel
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
             const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
     using C = BwdCfg<D>;
@@ -325,9 +355,9 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int i0 = p.causal ? key0 / kT : 0;
     const int nq = mtiles > i0 ? mtiles - i0 : 0;
     const uint32_t tmem = bwd_setup<D>(c, misc);
-    if (warp < 8) {
+    if (warp < C::TMA_WARP) {
         // Thread t of warpgroup wg owns key key0 + t (tensor-memory lane t)
-        // and columns [32 wg, 32 wg + 32) of every 64-query half.
+        // and columns [W wg, W wg + W) of every 64-query half.
         const int wg = warp >> 2, t = threadIdx.x & 127;
         const int key = key0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
@@ -337,7 +367,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         for (int g = 0; g < 2 * nq && ok; ++g) {
             const int k = g >> 1, h = g & 1, b = g & 1;   // query tile, half, S/dP buffer
             const int s = k % C::STAGES;
-            const int q0 = (i0 + k) * kT + h * C::HALF_ROWS + 32 * wg;   // this share's first query
+            const int q0 = (i0 + k) * kT + h * C::HALF_ROWS + C::W * wg;   // this share's first query
             // The stage's LSE2 / Dl arrived with its tiles (FULL), which the
             // MMA thread waited for before S_FULL; wait here too so that the
             // copies are visible to this thread.
@@ -347,12 +377,12 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             }
             tc_fence_after();
             const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) +
-                              h * C::HALF_ROWS + 32 * wg;
+                              h * C::HALF_ROWS + C::W * wg;
             const float* dl = l2 + kT;
             // Visible queries: column c with q0 + c >= key (causal); rows past
             // M have L2 = +inf; a key past N sees nothing.
             const int lo = p.causal ? key - q0 : 0;
-            const int hi = key < p.N ? 32 : 0;
+            const int hi = key < p.N ? C::W : 0;
             ok = rebuild_share<D, true, true>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs, l2, dl,
                                               0.f, 0.f, lo, hi);
         }
@@ -360,15 +390,18 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             ok = c.wait_warp(C::DONE, 0);
             tc_fence_after();
         }
-        if (ok) {   // warpgroup 0 writes dV, warpgroup 1 dK
+        if (ok) {   // the first half of the warpgroups writes dV, the second dK, each a share of the chunks
             const bool in = key < p.N;
             const int64_t off = (static_cast<int64_t>(bh) * p.N + key) * D;
-            if (wg == 0)
-                store_acc_row<D>(tm + C::TACC, nq > 0, in, p.dv + off, 1.f);
+            constexpr int kHalfWg = C::NWG / 2, kPer = (D / 32 + kHalfWg - 1) / kHalfWg;
+            const int part = wg % kHalfWg;
+            const int clo = min(D / 32, part * kPer), chi = min(D / 32, clo + kPer);
+            if (wg < kHalfWg)
+                store_acc_row<D>(tm + C::TACC, nq > 0, in, p.dv + off, 1.f, clo, chi);
             else
-                store_acc_row<D>(tm + C::TACC + D, nq > 0, in, p.dk + off, p.scale);
+                store_acc_row<D>(tm + C::TACC + D, nq > 0, in, p.dk + off, p.scale, clo, chi);
         }
-    } else if (warp == kTmaWarp) {
+    } else if (warp == C::TMA_WARP) {
         if ((threadIdx.x & 31) == 0 && nq > 0)
             bwd_producer<D>(c, s0, &map_k, &map_v, key0, &map_q, &map_do, i0 * kT, nq, bh, p.lse2, p.delta,
                             static_cast<int64_t>(bh) * p.Mpad + i0 * kT);
@@ -417,7 +450,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 
 // --------------------------------------------------------------- dQ kernel
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
     using C = BwdCfg<D>;
@@ -438,9 +471,9 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     const int kend = p.causal ? min(p.N, min(p.M, r0 + kT)) : p.N;
     const int nk = (kend + kT - 1) / kT;
     const uint32_t tmem = bwd_setup<D>(c, misc);
-    if (warp < 8) {
+    if (warp < C::TMA_WARP) {
         // Thread t of warpgroup wg owns query row r0 + t (tensor-memory lane
-        // t) and columns [32 wg, 32 wg + 32) of every 64-key half.
+        // t) and columns [W wg, W wg + W) of every 64-key half.
         const int wg = warp >> 2, t = threadIdx.x & 127;
         const int row = r0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
@@ -457,7 +490,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
                 break;
             }
             tc_fence_after();
-            const int hi = lim - (g * C::HALF_ROWS + 32 * wg);   // this share's keys: g * 64 + 32 wg + column
+            const int hi = lim - (g * C::HALF_ROWS + C::W * wg);   // this share's keys: g * 64 + W wg + column
             ok = rebuild_share<D, false, false>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs,
                                                 nullptr, nullptr, l2, dl, 0, hi);
         }
@@ -465,10 +498,13 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
             ok = c.wait_warp(C::DONE, 0);
             tc_fence_after();
         }
-        if (ok)   // each warpgroup writes half of the row's 32-column chunks
+        if (ok) {   // each warpgroup writes a share of the row's 32-column chunks
+            constexpr int kPer = (D / 32 + C::NWG - 1) / C::NWG;
+            const int clo = min(D / 32, wg * kPer), chi = min(D / 32, clo + kPer);
             store_acc_row<D>(tm + C::TACC, nk > 0, row < p.M, p.dq + (static_cast<int64_t>(bh) * p.M + row) * D,
-                             p.scale, wg == 0 ? 0 : (D / 32 + 1) / 2, wg == 0 ? (D / 32 + 1) / 2 : D / 32);
-    } else if (warp == kTmaWarp) {
+                             p.scale, clo, chi);
+        }
+    } else if (warp == C::TMA_WARP) {
         if ((threadIdx.x & 31) == 0 && nk > 0)
             bwd_producer<D>(c, s0, &map_q, &map_do, r0, &map_k, &map_v, 0, nk, bh, nullptr, nullptr, 0);
     } else if ((threadIdx.x & 31) == 0) {
@@ -525,11 +561,11 @@ cudaError_t launch_bwd_tc_t(const CUtensorMap& q, const CUtensorMap& k, const CU
         attr_set = true;
     }
     if (kv_blocks > 0) {
-        bwd_tc_dkdv<D><<<static_cast<unsigned>(kv_blocks), kThreads, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
+        bwd_tc_dkdv<D><<<static_cast<unsigned>(kv_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    bwd_tc_dq<D><<<static_cast<unsigned>(q_blocks), kThreads, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
+    bwd_tc_dq<D><<<static_cast<unsigned>(q_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
     return cudaGetLastError();
 }
 

@@ -382,6 +382,36 @@ def test_bwd_matches_oracle(B, H, M, N, D, causal):
         _check_grad(g.cpu().numpy(), r, f"{name} B{B} H{H} M{M} N{N} D{D} causal={causal}")
 
 
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_bwd_empty_keys_and_queries(D):
+    """N = 0: no key, dQ = 0 (and nothing else written); M = 0: no query, dK =
+    dV = 0. Both on the tensor-core path (D = 64, 128) and the CUDA-core one."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    B, H, M, N = 1, 2, 130, 70
+    bf = dict(device="cuda", dtype=torch.bfloat16)
+    q, do, o = (torch.randn(B, H, M, D, **bf) for _ in range(3))
+    k0 = torch.empty(B, H, 0, D, **bf)
+    lse = torch.full((B, H, M), float("-inf"), device="cuda")
+    dq = torch.full((B, H, M, D), float("nan"), device="cuda")
+    dk0 = torch.empty(B, H, 0, D, device="cuda")
+    fa.fa_bwd(q, k0, k0, o, lse, do, dq, dk0, dk0, D ** -0.5, False)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((dq == 0).all())
+    k, v = (torch.randn(B, H, N, D, **bf) for _ in range(2))
+    q0 = torch.empty(B, H, 0, D, **bf)
+    lse0 = torch.empty(B, H, 0, device="cuda")
+    dq0 = torch.empty(B, H, 0, D, device="cuda")
+    dk, dv = (torch.full((B, H, N, D), float("nan"), device="cuda") for _ in range(2))
+    fa.fa_bwd(q0, k, v, q0, lse0, q0, dq0, dk, dv, D ** -0.5, True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((dk == 0).all()) and bool((dv == 0).all())
+
+
 @pytest.mark.parametrize("name,heads", [("causal_b8_h32_s4096_d128", (0, 255)),
                                         ("gpt2m_b64_h16_s1024_d64", (0, 517, 1023))])
 def test_bwd_full_size_sampled_heads(name, heads):
