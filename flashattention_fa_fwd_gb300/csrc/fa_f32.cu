@@ -3,12 +3,15 @@
 // The single-head fp32 problem of "FlashAttention in Triton: A Tile-by-Tile
 // Walkthrough" (its kernel computes both dots in IEEE fp32 and streams key
 // tiles through a running max, sum and accumulator), generalised to a
-// [B, H] batch and the top-left causal mask. Each thread owns one query row;
-// a block stages 32-key tiles of K and V in shared memory, and every thread
-// runs the streaming softmax of "FlashAttention-style kernel" (section "The
-// loop") over them, with log2(e) folded into the scale and exp2f. Products
-// are plain fp32 fused multiply-adds (no TF32, no tensor cores); the final
-// division is IEEE.
+// [B, H] batch and the top-left causal mask, with the streaming softmax of
+// "FlashAttention-style kernel" (section "The loop": exp2 with log2(e) folded
+// into the scale) over 32-key tiles of K and V staged in shared memory.
+// Products are plain fp32 fused multiply-adds (no TF32), dot products over D
+// in order; the final division is IEEE. Two kernels:
+//   fa_fwd_f32_rows:  one thread per query row (many rows);
+//   fa_fwd_f32_warps: one warp per query row (few rows): the lanes take one
+//                     key each for the score, the warp updates the running
+//                     max and sum, then the lanes split D for acc += p V.
 //
 // Compiled without fast-math: exp2f and log2f are the full-accuracy CUDA
 // functions.
@@ -23,12 +26,14 @@ namespace fa {
 
 namespace {
 
-constexpr int kRows = 64;    // query rows (threads) per block
+constexpr int kRows = 64;    // query rows (threads) per block of the thread-per-row kernel
 constexpr int kKeys = 32;    // keys per shared-memory tile
+
+// Thread per row, for problems with enough rows to fill the GPU.
 
 template <int DMAX>
 __global__ void __launch_bounds__(kRows)
-fa_fwd_f32_kernel(const F32Params p, bool causal) {
+fa_fwd_f32_rows(const F32Params p, bool causal) {
     extern __shared__ float sm[];
     float* sK = sm;                    // [kKeys][DMAX]
     float* sV = sm + kKeys * DMAX;     // [kKeys][DMAX]
@@ -109,9 +114,9 @@ fa_fwd_f32_kernel(const F32Params p, bool causal) {
 }
 
 template <int DMAX>
-cudaError_t launch_f32_t(const F32Params& p, bool causal, cudaStream_t s) {
+cudaError_t launch_rows_t(const F32Params& p, bool causal, cudaStream_t s) {
     const int smem = 2 * kKeys * DMAX * static_cast<int>(sizeof(float));
-    auto kern = fa_fwd_f32_kernel<DMAX>;
+    auto kern = fa_fwd_f32_rows<DMAX>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -122,12 +127,153 @@ cudaError_t launch_f32_t(const F32Params& p, bool causal, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+constexpr int kWarps = 4;    // query rows (warps) per block of the warp-per-row kernel
+
+// Warp per row, for problems with too few rows to fill the GPU one thread per
+// row. K/V tiles are double-buffered: the next tile's loads are in flight
+// (in registers) while the current one is used.
+template <int DMAX>
+__global__ void __launch_bounds__(kWarps * 32)
+fa_fwd_f32_warps(const F32Params p, bool causal) {
+    constexpr int LD = DMAX + 4;       // padded row: distinct rows hit distinct banks
+    constexpr int PER = kKeys * DMAX / (kWarps * 32);   // tile elements per thread
+    extern __shared__ float sm[];
+    float* sK = sm;                    // [2][kKeys][LD]
+    float* sV = sK + 2 * kKeys * LD;   // [2][kKeys][LD]
+    float* sQ = sV + 2 * kKeys * LD;   // [kWarps][DMAX]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_blocks = (p.M + kWarps - 1) / kWarps;
+    const int bh = blockIdx.x / row_blocks;
+    const int row0 = (blockIdx.x - bh * row_blocks) * kWarps;
+    const int row = row0 + warp;
+    const bool valid = row < p.M;
+    const int D = p.D;
+    const float* qh = p.q + static_cast<size_t>(bh) * p.M * D;
+    const float* kh = p.k + static_cast<size_t>(bh) * p.N * D;
+    const float* vh = p.v + static_cast<size_t>(bh) * p.N * D;
+
+    float* q = sQ + warp * DMAX;
+    for (int d = lane; d < DMAX; d += 32) q[d] = (valid && d < D) ? qh[static_cast<size_t>(row) * D + d] : 0.f;
+    constexpr int DL = DMAX / 32;      // output columns per lane: lane + 32 i
+    float acc[DL];
+#pragma unroll
+    for (int i = 0; i < DL; ++i) acc[i] = 0.f;
+    const float c = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    // Keys any row of this block can see.
+    int n_keys = p.N;
+    if (causal) n_keys = min(n_keys, min(row0 + kWarps, p.M));
+
+    // Tile loads: element e = threadIdx.x + 128 i of the tile (row e / DMAX,
+    // column e % DMAX), coalesced along the rows.
+    float rk[PER], rv[PER];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = threadIdx.x + i * kWarps * 32, kr = e / DMAX, d = e % DMAX;
+            const bool in = (k0 + kr < p.N) && d < D;
+            rk[i] = in ? kh[static_cast<size_t>(k0 + kr) * D + d] : 0.f;
+            rv[i] = in ? vh[static_cast<size_t>(k0 + kr) * D + d] : 0.f;
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = threadIdx.x + i * kWarps * 32, kr = e / DMAX, d = e % DMAX;
+            sK[(buf * kKeys + kr) * LD + d] = rk[i];
+            sV[(buf * kKeys + kr) * LD + d] = rv[i];
+        }
+    };
+    if (n_keys > 0) {
+        load(0);
+        store(0);
+    }
+    __syncthreads();
+    for (int k0 = 0, buf = 0; k0 < n_keys; k0 += kKeys, buf ^= 1) {
+        const bool more = k0 + kKeys < n_keys;
+        if (more) load(k0 + kKeys);    // in flight while this tile is used
+        const float* tk = sK + buf * kKeys * LD;
+        const float* tv = sV + buf * kKeys * LD;
+
+        // Score of key k0 + lane: q . k over d in order.
+        const float4* q4 = reinterpret_cast<const float4*>(q);
+        const float4* k4 = reinterpret_cast<const float4*>(tk + lane * LD);
+        float dot = 0.f;
+#pragma unroll
+        for (int d4 = 0; d4 < DMAX / 4; ++d4) {
+            const float4 a = q4[d4], b = k4[d4];
+            dot = fmaf(a.x, b.x, dot);
+            dot = fmaf(a.y, b.y, dot);
+            dot = fmaf(a.z, b.z, dot);
+            dot = fmaf(a.w, b.w, dot);
+        }
+        const int key = k0 + lane;
+        const bool vis = key < p.N && (!causal || key <= row);
+        const float s = vis ? dot * c : -INFINITY;
+        float mx = s;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;   // fully masked so far
+        const float alpha = exp2f(m_run - m_use);
+        const float pl = exp2f(s - m_use);
+        float psum = pl;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+        l_run = l_run * alpha + psum;
+        // acc += p V over the tile's keys in order; lane owns columns lane + 32 i.
+#pragma unroll
+        for (int i = 0; i < DL; ++i) acc[i] *= alpha;
+#pragma unroll 8
+        for (int j = 0; j < kKeys; ++j) {
+            const float pj = __shfl_sync(0xffffffffu, pl, j);
+#pragma unroll
+            for (int i = 0; i < DL; ++i) acc[i] = fmaf(pj, tv[j * LD + lane + 32 * i], acc[i]);
+        }
+        m_run = m_new;
+        if (more) store(buf ^ 1);      // the other buffer was last read a tile ago
+        __syncthreads();
+    }
+
+    if (valid) {
+        float* orow = p.o + (static_cast<size_t>(bh) * p.M + row) * D;
+#pragma unroll
+        for (int i = 0; i < DL; ++i) {
+            const int d = lane + 32 * i;
+            if (d < D) orow[d] = (l_run > 0.f) ? acc[i] / l_run : 0.f;
+        }
+        if (lane == 0)
+            p.lse[static_cast<size_t>(bh) * p.M + row] =
+                (l_run > 0.f) ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    }
+}
+
+template <int DMAX>
+cudaError_t launch_warps_t(const F32Params& p, bool causal, cudaStream_t s) {
+    const int smem = (4 * kKeys * (DMAX + 4) + kWarps * DMAX) * static_cast<int>(sizeof(float));
+    auto kern = fa_fwd_f32_warps<DMAX>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    const long long blocks = static_cast<long long>((p.M + kWarps - 1) / kWarps) * p.bh_count;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(p, causal);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
+// Thread per row once there are enough rows for four blocks on every SM;
+// warp per row below that, where the thread-per-row kernel would leave most
+// SMs idle and wait on its long dependent dot products.
 cudaError_t launch_f32(const F32Params& p, bool causal, cudaStream_t s) {
-    if (p.D <= 32) return launch_f32_t<32>(p, causal, s);
-    if (p.D <= 64) return launch_f32_t<64>(p, causal, s);
-    return launch_f32_t<128>(p, causal, s);
+    const bool many = static_cast<long long>(p.bh_count) * p.M >= 152LL * 4 * kRows;
+    if (p.D <= 32) return many ? launch_rows_t<32>(p, causal, s) : launch_warps_t<32>(p, causal, s);
+    if (p.D <= 64) return many ? launch_rows_t<64>(p, causal, s) : launch_warps_t<64>(p, causal, s);
+    return many ? launch_rows_t<128>(p, causal, s) : launch_warps_t<128>(p, causal, s);
 }
 
 }  // namespace fa
