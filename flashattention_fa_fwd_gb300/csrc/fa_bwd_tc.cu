@@ -46,6 +46,7 @@ struct BwdCfg {
     // at D = 64 as well as at D = 128.)
     static constexpr int NWG = 2;
     static constexpr int W = 64 / NWG;
+    static_assert(W == 32, "the rebuild moves 32 columns per tensor-memory load");
     static constexpr int TMA_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1;
     static constexpr int THREADS = 32 * (4 * NWG + 2);
     static constexpr int PANELS = (D + 63) / 64;         // 64-column TMA boxes per tile row
@@ -160,32 +161,6 @@ __device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool i
     }
 }
 
-// Tensor-memory loads of 16 and stores of 8 consecutive columns (32 lanes x
-// 32-bit pattern), for the narrower rebuild shares.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[W]) {
-    if constexpr (W == 32) tmem_ld_x32(taddr, r);
-    else tmem_ld16(taddr, r);
-}
-template <int W>
-__device__ __forceinline__ void tmem_st_pairs(uint32_t taddr, const uint32_t (&r)[W / 2]) {
-    if constexpr (W == 32) tmem_st_x16(taddr, r);
-    else tmem_st8(taddr, r);
-}
-
 // Rebuilds W columns of this thread's row of P and dS from S and dP in
 // tensor memory: p = exp2(s * cs - L2), zero outside columns [lo, hi) of the
 // share when MASK; ds = p (dp - Dl). L2 and Dl are per column (dK/dV kernel,
@@ -235,8 +210,8 @@ __device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int b, in
     using C = BwdCfg<D>;
     constexpr int W = C::W;
     uint32_t sr[W], dr[W], pp[W / 2], dd[W / 2];
-    tmem_ld_cols<W>(ts + W * wg, sr);
-    tmem_ld_cols<W>(tdp + W * wg, dr);
+    tmem_ld_x32(ts + W * wg, sr);
+    tmem_ld_x32(tdp + W * wg, dr);
     tmem_ld_wait(sr);
     tmem_ld_wait(dr);
     tc_fence_before();
@@ -249,8 +224,8 @@ __device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int b, in
         if (!c.wait_warp(C::S_READ + b, phase)) return false;
         tc_fence_after();
     }
-    if (WRITE_P) tmem_st_pairs<W>(ts + (W / 2) * wg, pp);
-    tmem_st_pairs<W>((WRITE_P ? tdp : ts) + (W / 2) * wg, dd);
+    if (WRITE_P) tmem_st_x16(ts + (W / 2) * wg, pp);
+    tmem_st_x16((WRITE_P ? tdp : ts) + (W / 2) * wg, dd);
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(c.bar(C::P_FULL + b));
@@ -552,17 +527,13 @@ cudaError_t launch_bwd_tc_t(const CUtensorMap& q, const CUtensorMap& k, const CU
     const int64_t kv_blocks = static_cast<int64_t>(p.bh_count) * ((p.N + kT - 1) / kT);
     const int64_t q_blocks = static_cast<int64_t>(p.bh_count) * (p.Mpad / kT);
     if (kv_blocks > 0x7fffffffLL || q_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_tc_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_tc_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // Set on every call: the attribute belongs to the current device's context.
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_tc_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     if (kv_blocks > 0) {
         bwd_tc_dkdv<D><<<static_cast<unsigned>(kv_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
-        const cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     bwd_tc_dq<D><<<static_cast<unsigned>(q_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);

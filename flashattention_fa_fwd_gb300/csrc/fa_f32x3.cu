@@ -551,12 +551,9 @@ cudaError_t launch_x3_t(const X3Params& p, cudaStream_t s) {
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(x3_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    // Set on every call: the attribute belongs to the current device's context.
+    const cudaError_t e = cudaFuncSetAttribute(x3_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     x3_fwd<D><<<static_cast<unsigned>(blocks), kThreads, C::SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
