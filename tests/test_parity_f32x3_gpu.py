@@ -157,3 +157,35 @@ def test_f32x3_matches_exact_fp32_path_and_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert (o1 - oe).abs().max().item() <= 1e-5
     assert (l1 - le).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("name,path,heads", [("f32_causal_b8_h32_s4096_d128", "x3", (0, 131, 255)),
+                                             ("f32_gpt2m_b64_h16_s1024_d64", "x3", (0, 517, 1023)),
+                                             ("f32_gpt2m_b64_h16_s1024_d64", "ieee", (0, 1023))])
+def test_f32_full_size_sampled_rows(name, path, heads):
+    """A whole fp32 benchmark workload on the GPU in the benchmark's launch
+    shape (the tensor-core path, or the exact one), checked on 256 sampled
+    rows of sampled heads against the oracle at the fp32 bound, and finite
+    everywhere."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from oracle import attention_rows
+    from flashattention_fa_fwd_gb300.inputs import head_tensor, sample_rows
+
+    w = WORKLOADS[name]
+    q, k, v = make_inputs(w)
+    tq, tk, tv = (torch.from_numpy(x).cuda() for x in (q, k, v))
+    del q, k, v
+    o = torch.empty_like(tq)
+    lse = torch.empty(w.B, w.H, w.M, device="cuda")
+    (fa.fa_fwd_f32x3 if path == "x3" else fa.fa_fwd_f32)(tq, tk, tv, o, lse, w.scale, w.causal)
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    o_np, lse_np = o.cpu().numpy(), lse.cpu().numpy()
+    for bh in heads:
+        b, h = divmod(bh, w.H)
+        rows = sample_rows(w.wid, bh, w.M, 256)
+        qh, kh, vh = (head_tensor(w.wid, t, bh, r, w.D, 1.0, w.dtype) for t, r in ((0, w.M), (1, w.N), (2, w.N)))
+        o_ref, lse_ref = attention_rows(qh, kh, vh, w.scale, w.causal, rows)
+        check_f32(o_np[b, h, rows], lse_np[b, h, rows], o_ref, lse_ref, f"{name} {path} head {bh}")
