@@ -607,7 +607,16 @@ SlotLayout slot_layout(int64_t hc, int64_t M, int64_t N, int64_t D) {
     return L;
 }
 
-int64_t default_chunk(int64_t bh) { return bh < 8 ? bh : (bh + 7) / 8; }
+// Heads per chunk when the caller leaves it to the library: up to eight
+// chunks, but none with less than ~32 MB of inputs (smaller chunks cost more
+// in per-chunk launches and copy latency than their overlap saves).
+int64_t default_chunk(int64_t bh, int64_t M, int64_t N, int64_t D) {
+    const int64_t in_bytes = bh * (M + 2 * N) * D * 2;
+    int64_t chunks = (in_bytes + (32ll << 20) - 1) / (32ll << 20);
+    chunks = chunks < 1 ? 1 : (chunks > 8 ? 8 : chunks);
+    if (chunks > bh) chunks = bh;
+    return (bh + chunks - 1) / chunks;
+}
 
 fa_status pipe_setup(int dev, HostPipe** out) {
     HostPipe& P = g_pipe[dev];
@@ -635,7 +644,7 @@ FA_API int64_t fa_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t M, int6
     if (B < 0 || H < 0 || M < 0 || N < 0 || D < 1 || heads_per_chunk < 0) return -1;
     const int64_t bh = B * H;
     if (bh == 0 || M == 0) return 0;
-    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh) : heads_per_chunk;
+    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh, M, N, D) : heads_per_chunk;
     if (hc > bh) hc = bh;
     return kHostSlots * slot_layout(hc, M, N, D).bytes;
 }
@@ -651,7 +660,7 @@ FA_API fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* 
     if (heads_per_chunk < 0) return fail(FA_ERR_INVALID_ARG, "heads_per_chunk must be >= 0");
     if (empty) return FA_OK;
     const int64_t bh = B * H;
-    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh) : heads_per_chunk;
+    int64_t hc = heads_per_chunk == 0 ? default_chunk(bh, M, N, D) : heads_per_chunk;
     if (hc > bh) hc = bh;
     const SlotLayout L = slot_layout(hc, M, N, D);
     if (workspace == nullptr || workspace_bytes < kHostSlots * L.bytes)

@@ -188,7 +188,8 @@ int fa_fwd_splitkv_suggest(int64_t B, int64_t H, int64_t M, int64_t N, int causa
  * `solve` writes a preallocated output) does not say where they live.
  *
  * The B*H heads are processed in chunks of `heads_per_chunk` (0 = the
- * library's choice: about an eighth of them) through two slots of a
+ * library's choice: up to eight chunks, none with less than ~32 MB of
+ * q, k, v) through two slots of a
  * caller-owned device workspace: while the kernel runs one chunk on
  * `stream`, the next chunk's q, k, v are copied in and the previous chunk's
  * o, lse copied out on two streams the library creates once per device.

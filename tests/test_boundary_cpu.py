@@ -132,8 +132,12 @@ def test_host_entry_workspace_size_and_checks(lib):
     hc, M, N, D = 3, 100, 300, 64
     slot = pad(hc * M * D * 2) + 2 * pad(hc * N * D * 2) + pad(hc * M * D * 2) + pad(hc * M * 4)
     assert fa.fa_fwd_host_workspace_bytes(2, 4, M, N, D, hc) == 2 * slot
-    # default chunk: an eighth of the heads (rounded up); never more heads than exist
-    assert fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 0) == fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 32)
+    # default chunk: up to eight chunks, none with less than 32 MiB of q, k, v; never more heads than exist
+    assert fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 0) == fa.fa_fwd_host_workspace_bytes(8, 32, M, N, D, 256)
+    assert (fa.fa_fwd_host_workspace_bytes(8, 32, 4096, 4096, 128, 0)
+            == fa.fa_fwd_host_workspace_bytes(8, 32, 4096, 4096, 128, 32))   # 805 MB in: eight chunks
+    assert (fa.fa_fwd_host_workspace_bytes(2, 8, 1000, 3000, 96, 0)
+            == fa.fa_fwd_host_workspace_bytes(2, 8, 1000, 3000, 96, 16))     # 21 MB in: one chunk
     assert fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, 50) == fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, 2)
     assert fa.fa_fwd_host_workspace_bytes(0, 2, M, N, D, 0) == 0
     assert fa.fa_fwd_host_workspace_bytes(1, 2, M, N, D, -1) == -1
