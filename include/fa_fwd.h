@@ -140,7 +140,8 @@ fa_status fa_fwd_f32x3(const float* q, const float* k, const float* v, float* o,
                        float scale, int causal, void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Workspace bytes fa_fwd_f32x3 needs: 16 bytes per (head, key, column) with
- * the keys padded to a multiple of 64 (-1 for negative sizes). Needs no GPU. */
+ * the keys padded to the kernel's key block, 64 for D >= 96 and 32 below
+ * (-1 for negative sizes). Needs no GPU. */
 int64_t fa_fwd_f32x3_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
 
 /*

@@ -178,8 +178,11 @@ def test_bwd_workspace_size_and_checks(lib):
 
 
 def test_f32x3_workspace_size_and_checks(lib):
-    # 16 bytes per (head, key, column), keys padded to a multiple of 64.
+    # 16 bytes per (head, key, column), keys padded to the key block (64 for D >= 96, 32 below).
     assert fa.fa_fwd_f32x3_workspace_bytes(2, 3, 100, 64) == 2 * 3 * 128 * 64 * 16
+    assert fa.fa_fwd_f32x3_workspace_bytes(1, 1, 33, 64) == 64 * 64 * 16
+    assert fa.fa_fwd_f32x3_workspace_bytes(1, 1, 33, 128) == 64 * 128 * 16
+    assert fa.fa_fwd_f32x3_workspace_bytes(1, 1, 65, 128) == 128 * 128 * 16
     assert fa.fa_fwd_f32x3_workspace_bytes(1, 1, 0, 64) == 0
     assert fa.fa_fwd_f32x3_workspace_bytes(-1, 1, 1, 64) == -1
     W = 64 * A
