@@ -71,6 +71,9 @@ def parse_args(argv=None):
                     help="do not flush L2 between timed steps even when a step's inputs fit in it")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward pass fa_bwd on the workload")
+    ap.add_argument("--per-config", choices=["auto", "on", "off"], default="auto",
+                    help="also time the other benchmark workloads after the headline one (auto: on for the "
+                         "default forward workload on one GPU)")
     return ap.parse_args(argv)
 
 
@@ -299,12 +302,14 @@ def reference_arm(args, w, rank, world):
     dt = time.perf_counter() - t0
     value = flops * steps / dt / 1e12
     sample = f"each step: {nrows} sampled query rows of head 0 of {w.name} (fp64 numpy oracle)"
+    model, blas = host_cpu()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(w.describe(), sample=sample),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": model, "blas": blas},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -312,6 +317,170 @@ def reference_arm(args, w, rank, world):
 
 
 # --------------------------------------------------------------- GPU arm
+
+# Dense bf16 tensor-core FLOPs per clock per SM: NVIDIA's published dense
+# BF16 figure for Blackwell (2.25 PFLOP/s per GPU) at its boost clock, which
+# is also what one tcgen05 128x128x16 MMA every 64 cycles delivers
+# (2 * 128 * 128 * 16 / 64). TF32 runs at half that rate.
+BF16_FLOP_PER_CLK_SM = 8192
+TF32_FLOP_PER_CLK_SM = 4096
+
+# Workloads timed after the headline one, in the same run (per_config).
+PER_CONFIG = ["f32_single_head_m256_n512_d64", "gpt2m_b64_h16_s1024_d64", "causal_b8_h32_s4096_d128",
+              "cross_b2_h8_m1000_n3000_d96_peaked", "long_causal_b1_h8_s65536_d64"]
+
+
+def spec_peak(sms: int, mhz: float, per_clk: int, what: str):
+    """SMs x SM clock x per-SM dense rate, in TFLOP/s, with its derivation."""
+    return sms * mhz * 1e6 * per_clk / 1e12, f"{sms} SMs x {mhz:.0f} MHz x {per_clk} dense {what} FLOP/clk/SM"
+
+
+def host_cpu():
+    """The host's CPU model and numpy's BLAS, for the CPU baseline."""
+    import platform
+
+    import numpy as np
+
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        model = platform.processor() or platform.machine()
+    blas = "unknown"
+    try:
+        b = np.__config__.CONFIG["Build Dependencies"]["blas"]
+        blas = f"{b.get('name')} {b.get('version')}"
+    except (AttributeError, KeyError, TypeError):
+        pass
+    return f"{model} ({platform.machine()})", blas
+
+
+def time_steps(step, steps, stream, dev, flush=None, local_rank=0, world=1):
+    """Runs exactly `steps` calls of step() between a barrier + synchronize
+    on each side, each bracketed by CUDA events on `stream` (after an L2
+    flush on the same stream when `flush` is given), with nvidia-smi
+    sampling the clocks. Returns (per-launch ms, total ms of the steps,
+    clocks)."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_begin.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total = sum(per_launch) if flush is not None else t_begin.elapsed_time(t_end)  # flushes are not the workload
+    return per_launch, total, clocks
+
+
+def launch_stats(per_launch):
+    return {"mean": statistics.mean(per_launch), "median": statistics.median(per_launch), "min": min(per_launch),
+            "n": len(per_launch)}
+
+
+def l2_note(flush, step_in_bytes):
+    if flush is None and step_in_bytes > 129e6:
+        return f"inputs larger than L2 ({step_in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
+    if flush is not None:
+        return (f"L2 flushed before every timed step (256 MiB written; inputs {step_in_bytes / 2**20:.1f} MiB); "
+                "value from the steps' own CUDA events")
+    return "inputs fit in L2 (warm, --warm)"
+
+
+def calibrate(step, stream, dev, target_ms, lo, hi):
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(5):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    per = e0.elapsed_time(e1) / 5
+    return int(min(hi, max(lo, math.ceil(target_ms / max(per, 1e-3)))))
+
+
+def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False, warm=False):
+    """One other workload of the benchmark, timed in the same run: at least
+    50 steps (about 0.4 s of device time), median and min per-launch time,
+    roofline against both denominators, clocks."""
+    import torch
+
+    from flashattention_fa_fwd_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[name]
+    bf16 = w.dtype == "bf16"
+    tdtype = torch.bfloat16 if bf16 else torch.float32
+    q, k, v = (torch.from_numpy(x).to(dev).to(tdtype) for x in make_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.M, dtype=torch.float32, device=dev)
+    api, splits = ("fa_fwd" if bf16 else "fa_fwd_f32"), 1
+    if splitkv:
+        splits = fa.fa_fwd_splitkv_suggest(w.B, w.H, w.M, w.N, w.causal)
+        ws = torch.empty(max(fa.fa_fwd_splitkv_workspace_bytes(w.B, w.H, w.M, w.D, splits), 16), dtype=torch.uint8,
+                         device=dev)
+        api = f"fa_fwd_splitkv ({splits} splits, the library's suggestion)"
+
+        def step():
+            fa.fa_fwd_splitkv(q, k, v, o, lse, w.scale, w.causal, num_splits=splits, workspace=ws)
+    elif bf16:
+        def step():
+            fa.fa_fwd(q, k, v, o, lse, w.scale, w.causal)
+    else:
+        def step():
+            fa.fa_fwd_f32(q, k, v, o, lse, w.scale, w.causal)
+    for _ in range(3):
+        step()
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise SystemExit(f"device status after the warm-up of {name}")
+    steps = calibrate(step, stream, dev, 400.0, 50, 5000)
+    step_in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = torch.empty(64 * 2**20, dtype=torch.float32, device=dev) if step_in_bytes <= 129e6 and not warm else None
+    per_launch, total, clocks = time_steps(step, steps, stream, dev, flush, local_rank)
+    if fa.fa_get_device_status() != fa.FA_OK:
+        raise SystemExit(f"device status after timing {name}")
+    ls = launch_stats(per_launch)
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    if bf16:
+        peak, bound = float(peaks["bf16_tflops"]), "tensor"
+        pspec, pspec_src = spec_peak(sms, mhz, BF16_FLOP_PER_CLK_SM, "bf16")
+    else:
+        peak, bound = sms * 128 * 2 * mhz * 1e6 / 1e12, "alu"
+        pspec, pspec_src = peak, f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x {mhz:.0f} MHz (fp32 FMA)"
+    achieved = w.flops / (ls["mean"] * 1e-3) / 1e12
+    l2 = l2_note(flush, step_in_bytes)
+    del q, k, v, o, lse, flush
+    torch.cuda.empty_cache()
+    return {
+        "value": w.flops * steps / (total * 1e-3) / 1e12, "unit": UNIT, "steps": steps, "api": api,
+        "dtype": w.dtype, "config": dict(w.describe(), kv_splits=splits, l2=l2),
+        "launch_ms": ls,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "achieved_median": w.flops / (ls["median"] * 1e-3) / 1e12,
+                     "peak_spec": pspec, "peak_spec_source": pspec_src, "frac_of_spec": achieved / pspec,
+                     "traffic": recorded_traffic(name) if bf16 and splits == 1 else None},
+        "clocks": clocks, "clocks_rejected": clocks_rejected(clocks),
+    }
+
 
 def gpu_arm(args, w, rank, world, local_rank):
     import numpy as np
@@ -330,6 +499,7 @@ def gpu_arm(args, w, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     fa.load_library()
     peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     bf16 = w.dtype == "bf16"
     tdtype = torch.bfloat16 if bf16 else torch.float32
@@ -383,16 +553,9 @@ def gpu_arm(args, w, rank, world, local_rank):
     if st != fa.FA_OK:
         raise SystemExit(f"device status after warm-up: {fa.fa_status_string(st)}")
 
-    # Calibrate the default step count to about one second of device time.
+    # Default step count: about one second of device time, at least 50 steps.
     if args.steps is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(5):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        per = e0.elapsed_time(e1) / 5
-        steps = int(min(5000, max(20, math.ceil(1000.0 / max(per, 1e-3)))))
+        steps = calibrate(step, stream, dev, 1000.0, 50, 5000)
         steps = int(max_over_ranks(float(steps), world, dev))
     else:
         steps = args.steps
@@ -405,34 +568,16 @@ def gpu_arm(args, w, rank, world, local_rank):
     flush = None
     if step_in_bytes <= 129e6 and not args.warm:
         flush = torch.empty(64 * 2**20, dtype=torch.float32, device=dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t_begin.record(stream)
-    for i in range(steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = sampler.stop()
-    elapsed_ms = t_begin.elapsed_time(t_end)
-    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    l2 = l2_note(flush, step_in_bytes)
+    per_launch, timed_ms, clocks = time_steps(step, steps, stream, dev, flush, local_rank, world)
     st = fa.fa_get_device_status()
     if st != fa.FA_OK:
         raise SystemExit(f"device status after the timed region: {fa.fa_status_string(st)}")
-    timed_ms = sum(per_launch) if flush is not None else elapsed_ms   # the flushes are not the workload
     max_ms = max_over_ranks(timed_ms, world, dev)
     value = whole_job_value(flops, steps, world, max_ms)
-    launch_ms = statistics.mean(per_launch)
-    achieved = flops / (launch_ms * 1e-3) / 1e12
+    ls = launch_stats(per_launch)
+    achieved = flops / (ls["mean"] * 1e-3) / 1e12
+    del flush
 
     # End to end through the public call with host buffers.
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -496,15 +641,37 @@ def gpu_arm(args, w, rank, world, local_rank):
     if rank != 0:
         return 0
 
+    # The other workloads, timed after the headline in the same run (one GPU).
+    per_config = None
+    want = args.per_config == "on" or (args.per_config == "auto" and world == 1 and args.workload == DEFAULT_WORKLOAD
+                                         and args.batch is None and not bwd and splits == 1)
+    if want:
+        del hq, hk, hv, ho, hl
+        e2e_step = ws_host = None   # drops the e2e step's device buffers
+        torch.cuda.empty_cache()
+        per_config = {}
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            per_config[name] = per_config_line(fa, name, dev, stream, peaks, sms, local_rank, warm=args.warm)
+            if name == "cross_b2_h8_m1000_n3000_d96_peaked":
+                per_config[name + "+splitkv"] = per_config_line(fa, name, dev, stream, peaks, sms, local_rank,
+                                                                splitkv=True, warm=args.warm)
+
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
     peak = float(peaks["bf16_tflops"])
+    pspec, pspec_src = spec_peak(sms, mhz, BF16_FLOP_PER_CLK_SM, "bf16")
     bound, peak_source = "tensor", (f"{peaks.get('source')} bf16_tflops (burst); sustained "
                                     f"{peaks.get('bf16_tflops_sustained')}")
     frac_sust = achieved / float(peaks.get("bf16_tflops_sustained", peak))
+    ach_scale = 1.0
     if x3:
         # Three TF32 products per matrix product: the tensor core executes 3x the attention
         # FLOPs, against the TF32 peak (measured bf16 x the nominal TF32 : BF16 ratio 1.1 : 2.25).
+        ach_scale = 3.0
         achieved *= 3.0
         peak = float(peaks["bf16_tflops"]) * 1.1 / 2.25
+        pspec, pspec_src = spec_peak(sms, mhz, TF32_FLOP_PER_CLK_SM, "tf32")
         peak_source = (f"{peaks.get('source')} bf16_tflops x 1.1/2.25 (nominal dense TF32 : BF16); achieved "
                        f"counts the 3 TF32 products per attention FLOP")
         frac_sust = achieved / (float(peaks.get("bf16_tflops_sustained", peak)) * 1.1 / 2.25)
@@ -516,36 +683,34 @@ def gpu_arm(args, w, rank, world, local_rank):
     elif not bf16 or bwd:
         # The fp32 path and the backward run on the CUDA cores (fp32 FMA, no tensor cores):
         # its ceiling is SMs x 128 fp32 lanes x 2 FLOP per FMA x max SM clock.
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        mhz = float(peaks.get("sm_max_mhz", 2070.0))
         peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        pspec, pspec_src = peak, f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x {mhz:.0f} MHz (fp32 FMA)"
         bound = "alu"
-        peak_source = f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x {mhz:.0f} MHz (fp32 FMA)"
+        peak_source = pspec_src
         frac_sust = None
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, secs, nrows, cores, desc = oracle_sample(w, args.cpu_seconds)
+        model, blas = host_cpu()
         cpu = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-               "seconds": secs}
+               "seconds": secs, "cpu_model": model, "blas": blas}
     line = {
         "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": max_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas x{world}", kv_splits=splits,
                        **({"f32_path": "x3 (fa_fwd_f32x3)" if x3 else "ieee (fa_fwd_f32)"} if not bf16 else {}),
-                       l2=(f"inputs larger than L2 ({step_in_bytes / 2**20:.0f} MiB read per step vs 129 MB L2)"
-                           if flush is None and step_in_bytes > 129e6 else
-                           f"L2 flushed before every timed step (256 MiB written; inputs {step_in_bytes / 2**20:.1f} MiB); "
-                           "value from the steps' own CUDA events" if flush is not None else
-                           "inputs fit in L2 (warm, --warm)")),
-        "pct_of_peak": 100.0 * value / world * (3.0 if x3 else 1.0) / peak,
+                       l2=l2),
+        "pct_of_peak": 100.0 * value / world * ach_scale / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
                      "traffic": (recorded_traffic(w.describe()["workload"]) if bf16 and splits == 1 and not bwd else
                                  recorded_traffic(w.describe()["workload"], "x3") if x3 else None),
                      "peak_source": peak_source,
                      "frac_of_sustained": frac_sust,
-                     "launch_ms": launch_ms},
+                     "peak_spec": pspec, "peak_spec_source": pspec_src, "frac_of_spec": achieved / pspec,
+                     "launch_ms": ls["mean"], "launch_ms_median": ls["median"], "launch_ms_min": ls["min"],
+                     "achieved_median": flops * ach_scale / (ls["median"] * 1e-3) / 1e12},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps, "api": e2e_api},
@@ -553,6 +718,8 @@ def gpu_arm(args, w, rank, world, local_rank):
         "clocks": clocks,
         "clocks_rejected": clocks_rejected(clocks),
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     return 0
 

@@ -122,7 +122,11 @@ def fa_fwd_f32x3_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
 def fa_fwd_noalloc_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, M: int, N: int, D: int,
                        scale: float, causal: bool, stream: int = 0) -> int:
     """Calls fa_fwd_noalloc (the bf16 forward whose scratch is a static
-    device array, for callers that cannot allocate); returns the status."""
+    device array, for callers that cannot allocate); returns the status.
+
+    Calls that overlap on the GPU share that array and race. A pipeline
+    timeout of this entry point stays recorded in the array's status word
+    until fa_get_device_status() reads it, as for fa_fwd."""
     return load_library().fa_fwd_noalloc(q, k, v, o, lse, B, H, M, N, D, float(scale), int(bool(causal)), stream)
 
 

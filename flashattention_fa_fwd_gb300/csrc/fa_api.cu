@@ -41,27 +41,43 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
-// Work-counter slots of the bf16 kernel's unit scheduler: each launch takes
-// the next slot in turn, so up to this many launches may run at once (on
-// different streams) without sharing a counter.
+// Work-counter slots of the bf16 kernel's unit scheduler. An ordinary launch
+// takes the next of kSchedSlots slots in turn; before it reuses a slot, its
+// stream waits for the event recorded after the slot's previous launch, so
+// two running launches never share a counter (a 65th launch in flight
+// queues behind the first instead). A launch captured into a CUDA graph
+// cannot wait on events recorded outside the capture: it takes the next of
+// kGraphSlots slots reserved for captured launches, which ordinary launches
+// never touch.
 constexpr int kSchedSlots = 64;
+constexpr int kGraphSlots = 64;
 struct DeviceState {
-    uint32_t status;                 // the device status word
+    uint32_t status;                   // the device status word
     uint32_t pad;
-    int sched[kSchedSlots][2];       // per launch: next unit, CTAs finished
+    int sched[kSchedSlots][2];         // per launch: next unit, CTAs finished
+    int graph_sched[kGraphSlots][2];   // the same, for launches captured into graphs
+};
+struct SlotRing {
+    std::mutex mu[kSchedSlots];        // held from a slot's wait to its event record
+    cudaEvent_t done[kSchedSlots] = {};// recorded after the slot's last launch
 };
 std::mutex g_mu;
 uint32_t* g_status_word[kMaxDevices] = {};
 DeviceState* g_state[kMaxDevices] = {};
+SlotRing g_slots[kMaxDevices];
 std::atomic<uint32_t> g_launch_seq[kMaxDevices];
+std::atomic<uint32_t> g_graph_seq[kMaxDevices];
 int g_arch[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// Device address, per device, of fa_fwd_noalloc's static scratch array
+// (looked up on that entry point's first call on the device); word 0 is its
+// status word, which fa_get_device_status also reads.
+uint32_t* g_noalloc_scratch_addr[kMaxDevices] = {};
 
 // Per-device set-up on first use: architecture check, device state (status
 // word, work counters), and the driver's tensor-map encoder (fetched through
-// the runtime, so the library does not link libcuda). *sched, when asked
-// for, receives the work-counter slot of this launch.
-fa_status device_setup(bool need_encoder, uint32_t** status_word, int** sched = nullptr) {
+// the runtime, so the library does not link libcuda).
+fa_status device_setup(bool need_encoder, uint32_t** status_word) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -97,10 +113,50 @@ fa_status device_setup(bool need_encoder, uint32_t** status_word, int** sched = 
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     *status_word = g_status_word[dev];
-    if (sched != nullptr) {
-        const uint32_t slot = g_launch_seq[dev].fetch_add(1, std::memory_order_relaxed) % kSchedSlots;
-        *sched = g_state[dev]->sched[slot];
+    return FA_OK;
+}
+
+// Runs launch(sched) -- one launch of the bf16 kernel on stream `s` -- with a
+// work-counter pair that no other running launch uses (device_setup must
+// have succeeded on the current device). Ordinary launches cycle through
+// kSchedSlots pairs: the stream first waits for the event recorded after the
+// pair's previous launch, and the event is recorded again after this one,
+// all under the slot's lock so that concurrent host threads cannot
+// interleave their waits and records. Launches captured into a graph cycle
+// through kGraphSlots pairs of their own without events (a capture cannot
+// wait on an event recorded outside it); a graph's launch keeps its pair for
+// every replay, so replays of the same graph must not overlap one another
+// (as for any graph whose nodes share memory).
+template <class Launch>
+fa_status with_sched_slot(cudaStream_t s, Launch&& launch) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    DeviceState* state = g_state[dev];
+    if (cs != cudaStreamCaptureStatusNone) {
+        const uint32_t slot = g_graph_seq[dev].fetch_add(1, std::memory_order_relaxed) % kGraphSlots;
+        return launch(state->graph_sched[slot]);
     }
+    const uint32_t slot = g_launch_seq[dev].fetch_add(1, std::memory_order_relaxed) % kSchedSlots;
+    SlotRing& ring = g_slots[dev];
+    std::lock_guard<std::mutex> lock(ring.mu[slot]);
+    if (ring.done[slot] == nullptr) {
+        e = cudaEventCreateWithFlags(&ring.done[slot], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            ring.done[slot] = nullptr;
+            return cuda_fail(e, "creating a work-counter event");
+        }
+    } else {
+        e = cudaStreamWaitEvent(s, ring.done[slot], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "waiting for the work counters' previous launch");
+    }
+    const fa_status st = launch(state->sched[slot]);
+    if (st != FA_OK) return st;
+    e = cudaEventRecord(ring.done[slot], s);
+    if (e != cudaSuccess) return cuda_fail(e, "recording the work counters' event");
     return FA_OK;
 }
 
@@ -189,8 +245,7 @@ fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* 
     const int64_t n_pairs = (M + 255) / 256;
     if (bh * n_pairs > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many query tiles for one launch");
     uint32_t* word = nullptr;
-    int* sched = nullptr;
-    st = device_setup(true, &word, &sched);
+    st = device_setup(true, &word);
     if (st != FA_OK) return st;
 
     CUtensorMap mq, mk, mv;
@@ -216,15 +271,16 @@ fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* 
     p.ws_lse = nullptr;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
-    p.sched = sched;
-    cudaError_t e;
-    switch (D) {
-        case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
-        case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
-        default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
-    return FA_OK;
+    return with_sched_slot(s, [&](int* sched) -> fa_status {
+        p.sched = sched;
+        cudaError_t e;
+        switch (D) {
+            case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
+            case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
+            default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
+        }
+        return e == cudaSuccess ? FA_OK : cuda_fail(e, "launching the bf16 kernel");
+    });
 }
 
 }  // namespace
@@ -308,22 +364,30 @@ FA_API fa_status fa_get_device_status(void* stream) {
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return FA_OK;
-    uint32_t* w;
+    // Two status words: the one in the library's device state (every entry
+    // point but fa_fwd_noalloc) and word 0 of fa_fwd_noalloc's static array.
+    // Reading and clearing them allocates nothing.
+    uint32_t* words[2];
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        w = g_status_word[dev];
+        words[0] = g_status_word[dev];
+        words[1] = g_noalloc_scratch_addr[dev];
     }
-    if (w == nullptr) return FA_OK;
     uint32_t h = 0;
-    e = cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
-    if (h != 0) {
-        e = cudaMemset(w, 0, sizeof(uint32_t));
-        if (e == cudaSuccess) e = cudaDeviceSynchronize();
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
-        if (h & fa::DEV_ERR_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting on its pipeline (status 0x%x)", h);
-        return fail(FA_ERR_CUDA, "device status word 0x%x", h);
+    for (uint32_t* w : words) {
+        if (w == nullptr) continue;
+        uint32_t x = 0;
+        e = cudaMemcpy(&x, w, sizeof(x), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+        if (x != 0) {
+            e = cudaMemset(w, 0, sizeof(uint32_t));
+            if (e == cudaSuccess) e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+            h |= x;
+        }
     }
+    if (h & fa::DEV_ERR_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting on its pipeline (status 0x%x)", h);
+    if (h != 0) return fail(FA_ERR_CUDA, "device status word 0x%x", h);
     return FA_OK;
 }
 
@@ -399,8 +463,7 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     const int64_t n_pairs = (M + 255) / 256;
     if (bh * n_pairs * num_splits > 0x7fffffffLL) return fail(FA_ERR_UNSUPPORTED, "too many work units for one launch");
     uint32_t* word = nullptr;
-    int* sched = nullptr;
-    st = device_setup(true, &word, &sched);
+    st = device_setup(true, &word);
     if (st != FA_OK) return st;
     CUtensorMap mq, mk, mv;
     if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
@@ -425,16 +488,19 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     p.ws_lse = p.ws_o + num_splits * bh * M * D;
     p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
-    p.sched = sched;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (D) {
-        case 64: e = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
-        case 96: e = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
-        default: e = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "launching the bf16 kernel");
-    e = fa::launch_combine(p.ws_o, p.ws_lse, o, lse, bh * M, static_cast<int>(D), num_splits, s);
+    st = with_sched_slot(s, [&](int* sched) -> fa_status {
+        p.sched = sched;
+        cudaError_t err;
+        switch (D) {
+            case 64: err = fa::launch_bf16_d64(mq, mk, mv, p, causal != 0, s); break;
+            case 96: err = fa::launch_bf16_d96(mq, mk, mv, p, causal != 0, s); break;
+            default: err = fa::launch_bf16_d128(mq, mk, mv, p, causal != 0, s); break;
+        }
+        return err == cudaSuccess ? FA_OK : cuda_fail(err, "launching the bf16 kernel");
+    });
+    if (st != FA_OK) return st;
+    cudaError_t e = fa::launch_combine(p.ws_o, p.ws_lse, o, lse, bh * M, static_cast<int>(D), num_splits, s);
     if (e != cudaSuccess) return cuda_fail(e, "launching the split merge");
     return FA_OK;
 }
@@ -460,15 +526,17 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
 // the address up with cudaGetSymbolAddress (with that device current) and
 // caches it, so that first call should come before any stream capture. All
 // calls share the array and it keeps the last call's contents: each call
-// clears the words the kernel expects to start at zero (cudaMemsetAsync on
-// the caller's stream, before the launch), and calls that overlap on the GPU
-// (concurrent streams, or several host threads) race on it.
+// clears the two scheduler counters the kernel expects to start at zero
+// (cudaMemsetAsync on the caller's stream, before the launch); the status
+// word (word 0) keeps a recorded failure until fa_get_device_status reads
+// and clears it. Calls that overlap on the GPU (concurrent streams, or
+// several host threads) race on the array: they share the unit counter, so
+// work units can be skipped or done twice and O and LSE can be wrong.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int kNoAllocScratchWords = 64;
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
-uint32_t* g_noalloc_scratch_addr[kMaxDevices] = {};
 
 // Words of scratch the bf16 kernel needs, whatever the problem size: its
 // status word (word 0) and the two counters of its unit scheduler (words 1
@@ -538,7 +606,9 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
         mv = mq;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(scratch, 0, kBf16ScratchWords * sizeof(uint32_t), s);
+    // Word 0, the status word, stays as it is until fa_get_device_status
+    // reads and clears it; the two scheduler counters must start at zero.
+    cudaError_t e = cudaMemsetAsync(scratch + 1, 0, (kBf16ScratchWords - 1) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch");
     fa::Bf16Params p;
     p.o = o;

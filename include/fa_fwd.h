@@ -40,13 +40,19 @@
  * synchronise; the results are ready when the stream reaches them.
  *
  * The library allocates nothing per call. On its first call on a device it
- * allocates one small block of device state for that device (520 bytes),
+ * allocates one small block of device state for that device (1032 bytes),
  * which it keeps until the process exits: a status word, into which
  * device-side failures (a pipeline wait that ran out of time) are OR-ed and
- * which fa_get_device_status() reads, and 64 pairs of work counters that
- * the bf16 kernel's CTAs use to claim work units. Each bf16 launch takes the
- * next pair in turn and leaves it at zero when it ends, so at most 64 bf16
- * launches (fa_fwd, fa_fwd_splitkv) may be running on a device at once.
+ * which fa_get_device_status() reads, and 128 pairs of work counters that
+ * the bf16 kernel's CTAs use to claim work units. Each bf16 launch (fa_fwd,
+ * fa_fwd_splitkv, fa_fwd_host) takes the next of 64 pairs in turn and leaves
+ * it at zero when it ends; before reusing a pair, the launch's stream waits
+ * for an event recorded after the pair's previous launch, so any number of
+ * launches may be in flight on any streams and host threads without two
+ * running launches sharing a pair (the 65th queues behind the first). A
+ * launch captured into a CUDA graph takes the next of the other 64 pairs
+ * and keeps it for every replay of the graph: replays of graphs that hold
+ * the same pair must not overlap (captures 1 and 65 on a device share one).
  *
  * Errors
  * ------
@@ -224,9 +230,11 @@ int64_t fa_fwd_host_workspace_bytes(int64_t B, int64_t H, int64_t M, int64_t N, 
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word. Returns FA_ERR_TIMEOUT if a kernel launched since the last call gave
- * up on a pipeline wait (its outputs are then undefined), FA_ERR_CUDA if the
- * synchronisation itself failed, FA_OK otherwise.
+ * words (the library's device state and, once fa_fwd_noalloc has run on the
+ * device, word 0 of its static array). Returns FA_ERR_TIMEOUT if a kernel
+ * launched since the last call gave up on a pipeline wait (its outputs are
+ * then undefined), FA_ERR_CUDA if the synchronisation itself failed, FA_OK
+ * otherwise.
  */
 fa_status fa_get_device_status(void* stream);
 
@@ -250,12 +258,15 @@ fa_status fa_get_device_status(void* stream);
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture. Every call clears the scratch words on
- * `stream` before its launch. All calls share the one array, so calls that
- * overlap on the GPU (other streams, other host threads) race on it. A
- * device-side pipeline timeout in this variant leaves O and LSE undefined
- * and is not reported by fa_get_device_status(), which reads fa_fwd's own
- * status word.
+ * first call before any stream capture. Every call clears the two work
+ * counters on `stream` before its launch. All calls share the one array, so
+ * calls that overlap on the GPU (other streams, other host threads) race on
+ * it: they share the work counters, so units of work can be skipped or done
+ * twice and O and LSE can be wrong. Keep such calls on one stream, or order
+ * them with events. A device-side pipeline timeout in this variant leaves O
+ * and LSE undefined and is OR-ed into word 0 of the array, which keeps it
+ * until fa_get_device_status() reads and clears it (that call reads both
+ * this word and fa_fwd's, with plain copies that allocate nothing).
  */
 fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                          int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,

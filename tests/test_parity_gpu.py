@@ -8,6 +8,7 @@ ragged cross-attention workload), plus properties that hold at any size.
 """
 
 import math
+import warnings
 
 import numpy as np
 import pytest
@@ -91,7 +92,14 @@ def test_bf16_ragged_cross_workload_all_outputs():
     q, k, v = make_inputs(w)
     o, lse = run_bf16(q, k, v, w.scale, w.causal)
     o_ref, lse_ref = attention(q, k, v, w.scale, w.causal)
-    check_bf16(o, lse, o_ref, lse_ref, w.name)
+    err_o, err_l = check_bf16(o, lse, o_ref, lse_ref, w.name)
+    # The raw figures next to the bound: the bf16 output format alone rounds
+    # |O| >= 4 by up to 0.0156, so a few elements may sit above 1e-2.
+    raw = np.abs(np.asarray(o, dtype=np.float64) - o_ref)
+    above = int((raw > 1e-2).sum())
+    # Reported as a warning so that it shows in a quiet pytest run's summary.
+    warnings.warn(f"{w.name}: O max-abs {err_o:.4e} ({above} of {raw.size} elements above 1e-2, all within "
+                  f"1e-2 + ulp_bf16/2); LSE max-abs {err_l:.4e}", UserWarning)
 
 
 def test_bf16_large_logits_many_tiles():
@@ -215,6 +223,43 @@ def test_bf16_back_to_back_launches_on_two_streams():
             assert torch.equal(o, o0) and torch.equal(lse, l0)
         o_ref, lse_ref = attention(q, k, v, scale, causal)
         check_bf16(o0.float().cpu().numpy(), l0.cpu().numpy(), o_ref, lse_ref, f"problem {i}")
+
+
+def test_bf16_many_launches_in_flight_on_eight_streams():
+    """More bf16 launches in flight than there are work-counter slots: 96
+    launches over 8 streams, enqueued without any synchronisation in
+    between (launches i and i + 64 take the same slot and sit on different
+    streams). The library makes a slot's next launch wait for its previous
+    one, so every output must equal a serial run's bits, and that run must
+    match the oracle. Outputs start as NaN, so a skipped unit shows."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from parity import to_device_bf16
+
+    B, H, M, N, D, causal = 1, 8, 1024, 1024, 128, True
+    q, k, v = (_rand((B, H, S, D), 90 + j) for j, S in enumerate((M, N, N)))
+    tq, tk, tv = (to_device_bf16(x) for x in (q, k, v))
+    scale = D ** -0.5
+    o_ser = torch.empty_like(tq)
+    l_ser = torch.empty(B, H, M, dtype=torch.float32, device="cuda")
+    fa.fa_fwd(tq, tk, tv, o_ser, l_ser, scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    o_ref, lse_ref = attention(q, k, v, scale, causal)
+    check_bf16(o_ser.float().cpu().numpy(), l_ser.cpu().numpy(), o_ref, lse_ref, "serial run")
+
+    streams = [torch.cuda.Stream() for _ in range(8)]
+    outs = [(torch.full_like(tq, float("nan")), torch.full((B, H, M), float("nan"), device="cuda"))
+            for _ in range(96)]
+    torch.cuda.synchronize()
+    for i, (o, lse) in enumerate(outs):
+        with torch.cuda.stream(streams[i // 12]):
+            fa.fa_fwd(tq, tk, tv, o, lse, scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    bad = [i for i, (o, lse) in enumerate(outs) if not (torch.equal(o, o_ser) and torch.equal(lse, l_ser))]
+    assert not bad, f"launches {bad} differ from the serial run"
 
 
 @pytest.mark.parametrize("B,H,M,N,D,causal,chunk", [(2, 5, 300, 700, 128, True, 0), (1, 7, 1000, 513, 64, False, 3),
