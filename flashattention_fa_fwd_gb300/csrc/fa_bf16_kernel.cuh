@@ -27,7 +27,8 @@
 //   WG2 (warps 8-11)  epilogue (O / l, LSE) of the previous unit while the
 //                     next one runs
 //   WG3 (warps 12-15) warp 12: TMA producer; warp 13: tensor-memory owner
-//                     and MMA issuer; warps 14-15 idle
+//                     and MMA issuer; warp 14: K/V gate (waits for K/V
+//                     tiles in the MMA thread's place); warp 15 idle
 //
 // Tensor memory (512 columns, 128 lanes, lane = query row of the tile):
 //   [  0,128)  S_0 (fp32 scores of tile 0); P_0 (bf16, packed in pairs)
@@ -51,11 +52,18 @@
 // when it enters P V -- is compensated by normalising O with l_o, which
 // counts each tile's largest weight as rounded.
 //
-// Hand-offs (mbarriers): S_FULL (MMA -> softmax), P_FULL (softmax -> MMA),
-// per unit ST_FULL / ST_EMPTY (softmax <-> epilogue: m, l, l_o), O_DONE
-// (MMA -> epilogue), O_FREE (epilogue -> MMA: O_t may be overwritten by the
-// next unit), Q_FULL / Q_EMPTY and KV_FULL / KV_EMPTY (TMA ring), UNIT_FULL /
-// UNIT_EMPTY (the ring of claimed unit indices).
+// Hand-offs (mbarriers): S_FULL (MMA -> softmax of tile 0), ITER (one MMA
+// commit per key tile step: announces S_1 to the softmax of tile 1 and frees
+// the step's K/V stages for the producer), P_FULL (softmax -> MMA; for tile 0
+// also the gate's "V(j-1) and K(j) have landed"), per unit ST_FULL /
+// ST_EMPTY (softmax <-> epilogue: m, l, l_o), O_DONE (MMA -> epilogue),
+// O_FREE (epilogue -> MMA: O_t may be overwritten by the next unit), Q_FULL /
+// Q_EMPTY and KV_FULL (TMA), UNIT_FULL / UNIT_EMPTY (the ring of claimed unit
+// indices). While the tensor core streams its operands from shared memory,
+// every mbarrier poll or commit of the MMA thread takes 100-160 cycles, during
+// which the tensor pipe (about three MMAs deep) runs dry; the thread
+// therefore makes only four such calls per step in the steady state (two P
+// waits, the S_0 commit and the step's ITER commit), none back to back.
 //
 // Causal (top-left, key j visible to query i when j <= i): key tiles wholly
 // above the diagonal are never loaded or multiplied; the diagonal tile and a
@@ -102,15 +110,20 @@ struct Bf16Cfg {
     static constexpr int STATS_OFF = KV_OFF + NS * TILE_BYTES;      // float [2 t][3 (m, l, l_o)][128]
     static constexpr int BAR_OFF = STATS_OFF + 2 * 3 * 128 * 4;
     // barrier slots
-    static constexpr int KV_FULL = 0, KV_EMPTY = NS, Q_FULL = 2 * NS, Q_EMPTY = 2 * NS + QB;
-    static constexpr int S_FULL = 2 * NS + 2 * QB, P_FULL = S_FULL + 2, O_DONE = S_FULL + 4;
-    static constexpr int O_FREE = S_FULL + 6, ST_FULL = S_FULL + 8, ST_EMPTY = S_FULL + 10;
-    static constexpr int DRAIN = S_FULL + 12;
+    // ITER: ring of per-iteration completion barriers (one MMA commit per key
+    // tile step); it releases K/V stages and announces S_1.
+    static constexpr int ITERS = 8;
+    static constexpr int KV_FULL = 0, ITER = NS, Q_FULL = NS + ITERS, Q_EMPTY = Q_FULL + QB;
+    static constexpr int S_FULL = Q_EMPTY + QB;                     // S_0 only
+    static constexpr int P_FULL = S_FULL + 1, O_DONE = P_FULL + 2;
+    static constexpr int O_FREE = O_DONE + 2, ST_FULL = O_FREE + 2, ST_EMPTY = ST_FULL + 2;
+    static constexpr int DRAIN = ST_EMPTY + 2;
     static constexpr int UNIT_SLOTS = 4;                            // ring of claimed unit indices
     static constexpr int UNIT_FULL = DRAIN + 1, UNIT_EMPTY = UNIT_FULL + UNIT_SLOTS;
-    // Readers of a ring slot: the MMA thread, and one lane of each of the
-    // four warps of both softmax warpgroups and of the epilogue warpgroup.
-    static constexpr int UNIT_READERS = 1 + 3 * 4;
+    // Readers of a ring slot: the MMA thread, one lane of each of the four
+    // warps of both softmax warpgroups and of the epilogue warpgroup, and the
+    // K/V gate thread.
+    static constexpr int UNIT_READERS = 1 + 3 * 4 + 1;
     static constexpr int NUM_BARS = UNIT_EMPTY + UNIT_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;         // tensor-memory base, abort flag
     static constexpr int RING_OFF = MISC_OFF + 16;                  // int [UNIT_SLOTS]
@@ -224,6 +237,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
     const uint64_t pol_q = policy_evict_first();
     const uint64_t pol_kv = policy_evict_last();
     int kv_idx = 0, qit = 0;
+    int it_base = 0;         // MMA iteration of the current unit's first key tile step
+    int rel[C::NS];          // per stage: the MMA iteration whose commit frees its last load
     bool ok = true;
     // Claims the CTA's next unit and publishes it in the ring (-1 once the
     // units are used up). A CTA's first unit is its own index (the grid
@@ -284,10 +299,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
             for (int which = 0; which < 2; ++which) {
                 const int stage = kv_idx % C::NS;
                 const int round = kv_idx / C::NS;
-                if (round > 0 && !c.wait(C::KV_EMPTY + stage, round - 1)) {
+                if (round > 0 && !c.wait(C::ITER + rel[stage] % C::ITERS, rel[stage] / C::ITERS)) {
                     ok = false;
                     break;
                 }
+                // K(j) is last read in step j of the unit, V(j) in step j + 1.
+                rel[stage] = it_base + j + which;
                 mbar_arrive_expect_tx(c.bar(C::KV_FULL + stage), C::TILE_BYTES);
                 const CUtensorMap* m = which ? mv : mk;
                 for (int pn = 0; pn < C::PANELS; ++pn)
@@ -296,6 +313,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* mq, const CUten
                 ++kv_idx;
             }
         }
+        it_base += U.nmax + 1;
         u = u_next;
     }
     // Every copy issued must land before this CTA's shared memory is
@@ -341,6 +359,7 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
             mma_ts(c.tmem + o_col, c.tmem + s_col + kk * 8, dv + kk * (2048 >> 4), id_o, (first && kk == 0) ? 0u : 1u);
     };
     int kv_idx = 0, qit = 0;
+    int itr = 0;            // key tile steps issued (one ITER commit each)
     int pv0 = 0, pv1 = 0;   // P V products issued per query tile
     int uo0 = 0, uo1 = 0;   // units whose last product was committed, per tile
     bool ok = true;
@@ -359,17 +378,22 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
         tc_fence_after();
         const uint64_t dq0 = desc_k + ((sq + (qb * 2 + 0) * C::TILE_BYTES) >> 4);
         const uint64_t dq1 = desc_k + ((sq + (qb * 2 + 1) * C::TILE_BYTES) >> 4);
-        // Key tile j: K(j) sits in ring slot kidx = kv_idx + 2j, V(j-1) in
-        // slot kidx - 1.
+        // Key tile step j: K(j) sits in ring slot kidx = kv_idx + 2j, V(j-1)
+        // in slot kidx - 1.
         for (int j = 0; j <= nm; ++j) {
             const int kidx = kv_idx + 2 * j;
             const int kst = kidx % C::NS, vst = (kidx + C::NS - 1) % C::NS;
             const uint64_t dk = desc_k + ((skv + kst * C::TILE_BYTES) >> 4);
             const uint64_t dv = desc_v + ((skv + vst * C::TILE_BYTES) >> 4);
-            // V(j-1) gates the P V products, K(j) only the Q K^T ones.
-            if (j >= 1 && !c.wait(C::KV_FULL + vst, (kidx - 1) / C::NS)) {
-                ok = false;
-                break;
+            // When tile 0 has a P V product in this step, its P_FULL phase
+            // also certifies V(j-1) and K(j) (the gate thread arrives on it
+            // once both have landed); otherwise wait for them here.
+            if (j == 0 || j > n0) {
+                if ((j >= 1 && !c.wait(C::KV_FULL + vst, (kidx - 1) / C::NS)) ||
+                    (j < nm && !c.wait(C::KV_FULL + kst, kidx / C::NS))) {
+                    ok = false;
+                    break;
+                }
             }
             if (j >= 1 && j <= n0) {
                 if (!c.wait(C::P_FULL + 0, pv0) || (j == 1 && uo0 > 0 && !c.wait(C::O_FREE + 0, uo0 - 1))) {
@@ -383,19 +407,11 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
                     mma_commit(c.bar(C::O_DONE + 0));
                     ++uo0;
                 }
-                // V(j-1) is free once its last product completes (a commit
-                // covers every MMA issued before it); tile 1, issued after
-                // tile 0, is its last user whenever it uses it at all.
-                if (j > n1) mma_commit(c.bar(C::KV_EMPTY + vst));
-            }
-            if (j < nm && !c.wait(C::KV_FULL + kst, kidx / C::NS)) {
-                ok = false;
-                break;
             }
             if (j < n0) {
                 tc_fence_after();
                 issue_s(C::S_COL0, dq0, dk);
-                mma_commit(c.bar(C::S_FULL + 0));
+                mma_commit(c.bar(C::S_FULL));
             }
             if (j >= 1 && j <= n1) {
                 if (!c.wait(C::P_FULL + 1, pv1) || (j == 1 && uo1 > 0 && !c.wait(C::O_FREE + 1, uo1 - 1))) {
@@ -409,15 +425,16 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
                     mma_commit(c.bar(C::O_DONE + 1));
                     ++uo1;
                 }
-                mma_commit(c.bar(C::KV_EMPTY + vst));
             }
             if (j < n1) {
                 tc_fence_after();
                 issue_s(C::S_COL1, dq1, dk);
-                mma_commit(c.bar(C::S_FULL + 1));
             }
-            if (j < nm) mma_commit(c.bar(C::KV_EMPTY + kst));
             if (j == nm - 1) mma_commit(c.bar(C::Q_EMPTY + qb));
+            // One commit per step: S_1(j) is ready, and K(j) and V(j-1) are
+            // free once every product issued so far has completed.
+            mma_commit(c.bar(C::ITER + itr % C::ITERS));
+            ++itr;
         }
         kv_idx += 2 * nm;
         ++qit;
@@ -439,12 +456,15 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
     const float cl2 = p.scale_log2;
     const uint64_t c2 = f2_pack(cl2, cl2);
     int s_cnt = 0, st_cnt = 0;
+    int it_base = 0;   // MMA step of the current unit's first key tile
     bool ok = true;
     UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
     while (ok) {
         const int u = units.next(c, true);
         if (u < 0) break;
         const Unit U = unit_info<CAUSAL>(u, p);
+        const int itb = it_base;
+        if (U.nmax > 0) it_base += U.nmax + 1;
         const int ntile = t ? U.n1 : U.n0;
         if (ntile == 0) continue;
         const int qt0 = U.q0 + 128 * t;                     // first row of the tile
@@ -455,7 +475,11 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
         for (int j = 0; j < ntile; ++j) {
             // Every lane must agree: the tensor-memory loads below are
             // warp-collective.
-            if (!c.wait_warp(C::S_FULL + t, s_cnt)) {
+            // S_0(j) has its own barrier; S_1(j) is announced by step j's
+            // ITER commit.
+            const bool s_ok = t == 0 ? c.wait_warp(C::S_FULL, s_cnt)
+                                     : c.wait_warp(C::ITER + (itb + j) % C::ITERS, (itb + j) / C::ITERS);
+            if (!s_ok) {
                 ok = false;
                 break;
             }
@@ -580,6 +604,41 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
         st[256 + r] = lo_run;
         c.arrive_warp(C::ST_FULL + t);
         ++st_cnt;
+    }
+}
+
+// ------------------------------------------------------------ K/V gate
+// Waits, in the MMA thread's place, for the K/V tiles of each step in which
+// query tile 0 has a P V product: step j + 1 reads V(j) and K(j + 1) (if
+// any), and the MMA thread waits on P_FULL_0 phase of tile j before it
+// issues anything in that step. The gate arrives on that phase (its 129th
+// arrival, next to the 128 softmax threads) once both tiles have landed,
+// then waits for the phase to complete before it arrives again. Shared-
+// memory polls are slow while the tensor core streams its operands, so
+// every one taken off the MMA thread leaves the tensor pipe fed longer.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void gate_role(const Bf16Params& p, const Ctx& c) {
+    using C = Bf16Cfg<D>;
+    int kv_idx = 0;   // loads issued before the current unit (the producer's count)
+    int pc = 0;       // P_FULL_0 phases
+    UnitReader<C::UNIT_SLOTS, C::UNIT_FULL, C::UNIT_EMPTY> units;
+    while (true) {
+        const int u = units.next(c, false);
+        if (u < 0) break;
+        const Unit U = unit_info<CAUSAL>(u, p);
+        if (U.nmax == 0) continue;
+        bool ok = true;
+        for (int j = 0; j < U.n0 && ok; ++j) {
+            const int lv = kv_idx + 2 * j + 1;   // V(j); K(j + 1) follows it
+            ok = c.wait(C::KV_FULL + lv % C::NS, lv / C::NS) &&
+                 (j + 1 >= U.nmax || c.wait(C::KV_FULL + (lv + 1) % C::NS, (lv + 1) / C::NS));
+            if (!ok) break;
+            mbar_arrive(c.bar(C::P_FULL + 0));
+            ok = c.wait(C::P_FULL + 0, pc);
+            ++pc;
+        }
+        if (!ok) break;
+        kv_idx += 2 * U.nmax;
     }
 }
 
@@ -711,17 +770,16 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(c.bar(C::KV_FULL + s), 1);
-            mbar_init(c.bar(C::KV_EMPTY + s), 1);
-        }
+        for (int s = 0; s < C::NS; ++s) mbar_init(c.bar(C::KV_FULL + s), 1);
+        for (int s = 0; s < C::ITERS; ++s) mbar_init(c.bar(C::ITER + s), 1);
         for (int b = 0; b < C::QB; ++b) {
             mbar_init(c.bar(C::Q_FULL + b), 1);
             mbar_init(c.bar(C::Q_EMPTY + b), 1);
         }
+        mbar_init(c.bar(C::S_FULL), 1);
+        mbar_init(c.bar(C::P_FULL + 0), 128 + 1);   // softmax of tile 0 + the K/V gate
+        mbar_init(c.bar(C::P_FULL + 1), 128);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(c.bar(C::S_FULL + t), 1);
-            mbar_init(c.bar(C::P_FULL + t), 128);
             mbar_init(c.bar(C::O_DONE + t), 1);
             mbar_init(c.bar(C::O_FREE + t), 128);
             mbar_init(c.bar(C::ST_FULL + t), 128);
@@ -762,6 +820,9 @@ fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_const
             __syncwarp();
         } else if (warp == 13) {
             if (lane == 0) mma_role<D, CAUSAL>(p, c);
+            __syncwarp();
+        } else if (warp == 14) {
+            if (lane == 0) gate_role<D, CAUSAL>(p, c);
             __syncwarp();
         }
     }
