@@ -419,7 +419,7 @@ def calibrate(step, stream, dev, target_ms, lo, hi):
     return int(min(hi, max(lo, math.ceil(target_ms / max(per, 1e-3)))))
 
 
-def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False, warm=False):
+def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False, warm=False, cpu_baseline=False):
     """One other workload of the benchmark, timed in the same run: at least
     50 steps (about 0.4 s of device time), median and min per-launch time,
     roofline against both denominators, clocks."""
@@ -430,7 +430,8 @@ def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False
     w = WORKLOADS[name]
     bf16 = w.dtype == "bf16"
     tdtype = torch.bfloat16 if bf16 else torch.float32
-    q, k, v = (torch.from_numpy(x).to(dev).to(tdtype) for x in make_inputs(w))
+    host = make_inputs(w)
+    q, k, v = (torch.from_numpy(x).to(dev).to(tdtype) for x in host)
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.M, dtype=torch.float32, device=dev)
     api, splits = ("fa_fwd" if bf16 else "fa_fwd_f32"), 1
@@ -470,6 +471,8 @@ def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False
     l2 = l2_note(flush, step_in_bytes)
     del q, k, v, o, lse, flush
     torch.cuda.empty_cache()
+    cpu = oracle_config_timing(w, host) if cpu_baseline else None
+    del host
     return {
         "value": w.flops * steps / (total * 1e-3) / 1e12, "unit": UNIT, "steps": steps, "api": api,
         "dtype": w.dtype, "config": dict(w.describe(), kv_splits=splits, l2=l2),
@@ -479,7 +482,48 @@ def per_config_line(fa, name, dev, stream, peaks, sms, local_rank, splitkv=False
                      "peak_spec": pspec, "peak_spec_source": pspec_src, "frac_of_spec": achieved / pspec,
                      "traffic": recorded_traffic(name) if bf16 and splits == 1 else None},
         "clocks": clocks, "clocks_rejected": clocks_rejected(clocks),
+        "cpu_baseline": cpu,
     }
+
+
+# Workloads whose oracle the per-config CPU baseline runs in full; the others
+# are timed on sampled query rows (the 64K-token workload: 256 rows of each
+# of its 8 heads, as its parity test) and extrapolated to the whole workload.
+CPU_FULL = ("f32_single_head_m256_n512_d64", "gpt2m_b64_h16_s1024_d64", "cross_b2_h8_m1000_n3000_d96_peaked")
+
+
+def oracle_config_timing(w, host):
+    """The fp64 oracle on this host's cores for workload w (inputs as the GPU
+    got them): in full where that takes seconds, else on sampled rows."""
+    import numpy as np
+
+    from flashattention_fa_fwd_gb300.inputs import sample_rows
+    from oracle import attention, attention_rows
+
+    q, k, v = host
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model, blas = host_cpu()
+    out = {"unit": UNIT, "cores": int(cores), "kind": "oracle", "cpu_model": model, "blas": blas}
+    if w.name in CPU_FULL:
+        t0 = time.perf_counter()
+        attention(q, k, v, w.scale, w.causal)
+        secs = time.perf_counter() - t0
+        out.update(value=w.flops / secs / 1e12, seconds=secs, sample=f"the whole workload ({w.name}, fp64 numpy oracle)")
+        return out
+    qf, kf, vf = (x.reshape(w.B * w.H, x.shape[-2], w.D) for x in (q, k, v))
+    flops, secs, nrows = 0.0, 0.0, 0
+    for bh in range(w.B * w.H):
+        rows = sample_rows(w.wid, bh, w.M, 256)
+        t0 = time.perf_counter()
+        attention_rows(qf[bh], kf[bh], vf[bh], w.scale, w.causal, rows)
+        secs += time.perf_counter() - t0
+        vis = np.minimum(rows + 1, w.N) if w.causal else np.full(rows.size, w.N)
+        flops += 4.0 * w.D * float(vis.sum())
+        nrows += int(rows.size)
+    out.update(value=flops / secs / 1e12, seconds=secs,
+               sample=f"{nrows} sampled query rows of {w.name} (256 per head, fp64 numpy oracle)",
+               extrapolated_full_seconds=secs * w.flops / flops)
+    return out
 
 
 def gpu_arm(args, w, rank, world, local_rank):
@@ -653,7 +697,8 @@ def gpu_arm(args, w, rank, world, local_rank):
         for name in PER_CONFIG:
             if name == w.name:
                 continue
-            per_config[name] = per_config_line(fa, name, dev, stream, peaks, sms, local_rank, warm=args.warm)
+            per_config[name] = per_config_line(fa, name, dev, stream, peaks, sms, local_rank, warm=args.warm,
+                                               cpu_baseline=not args.no_cpu_baseline)
             if name == "cross_b2_h8_m1000_n3000_d96_peaked":
                 per_config[name + "+splitkv"] = per_config_line(fa, name, dev, stream, peaks, sms, local_rank,
                                                                 splitkv=True, warm=args.warm)
