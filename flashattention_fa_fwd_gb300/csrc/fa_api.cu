@@ -200,11 +200,11 @@ fa_status validate(const void* q, const void* k, const void* v, const void* o, c
     return FA_OK;
 }
 
-// 3-D {D, rows, B*H} bf16 map, 128-row x 64-column box, 128-byte swizzle.
-fa_status encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t bh, int64_t D) {
+// 3-D {D, rows, B*H} bf16 map, box_rows x 64-column box, 128-byte swizzle.
+fa_status encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t bh, int64_t D, int box_rows = 128) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(bh)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(rows * D * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t elem_strides[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                           elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -251,8 +251,8 @@ fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* 
     CUtensorMap mq, mk, mv;
     if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
     if (N > 0) {
-        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
-        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mk, k, N, bh, D, fa::kv_box_rows(D, 1))) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D, fa::kv_box_rows(D, 1))) != FA_OK) return st;
     } else {
         mk = mq;  // never read: no key tiles exist
         mv = mq;
@@ -468,8 +468,8 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     CUtensorMap mq, mk, mv;
     if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
     if (N > 0) {
-        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
-        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mk, k, N, bh, D, fa::kv_box_rows(D, num_splits))) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D, fa::kv_box_rows(D, num_splits))) != FA_OK) return st;
     } else {
         mk = mq;
         mv = mq;
@@ -599,8 +599,8 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
     CUtensorMap mq, mk, mv;
     if ((st = encode_map(&mq, q, M, bh, D)) != FA_OK) return st;
     if (N > 0) {
-        if ((st = encode_map(&mk, k, N, bh, D)) != FA_OK) return st;
-        if ((st = encode_map(&mv, v, N, bh, D)) != FA_OK) return st;
+        if ((st = encode_map(&mk, k, N, bh, D, fa::kv_box_rows(D, 1))) != FA_OK) return st;
+        if ((st = encode_map(&mv, v, N, bh, D, fa::kv_box_rows(D, 1))) != FA_OK) return st;
     } else {
         mk = mq;
         mv = mq;

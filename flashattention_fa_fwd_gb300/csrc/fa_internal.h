@@ -33,8 +33,12 @@ struct Bf16Params {
 };
 
 // Launches the bf16 kernel for head dimension D (64, 96 or 128); the three
-// maps are 3-D {D, rows, B*H} bf16 maps with a {64, 128, 1} box and 128-byte
-// swizzle. Returns the launch error.
+// maps are 3-D {D, rows, B*H} bf16 maps with a {64, rows, 1} box and 128-byte
+// swizzle: 128 rows for Q, and for K and V except at D = 64 without key
+// splits (kv_box_rows), whose kernel streams 64-key tiles. Returns the launch
+// error.
+constexpr int kv_box_rows(int64_t D, int splits) { return (D == 64 && splits == 1) ? 64 : 128; }
+
 cudaError_t launch_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const Bf16Params& p, bool causal, cudaStream_t s);
 cudaError_t launch_bf16_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
