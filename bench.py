@@ -139,7 +139,7 @@ class ClockSampler:
 
 # Sources of each path's kernels; a recorded ncu traffic figure is reported
 # only while these hash to the value it was taken with.
-KERNEL_SOURCES = ["fa_bf16_kernel.cuh", "ptx.cuh", "fa_internal.h", "fa_api.cu",
+KERNEL_SOURCES = ["fa_bf16_kernel.cuh", "fa_bf16_q1.cuh", "ptx.cuh", "fa_internal.h", "fa_api.cu",
                   "fa_bf16_d64.cu", "fa_bf16_d96.cu", "fa_bf16_d128.cu"]
 X3_SOURCES = ["fa_f32x3.cu", "ptx.cuh", "fa_internal.h", "fa_api.cu"]
 PROFILES = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
