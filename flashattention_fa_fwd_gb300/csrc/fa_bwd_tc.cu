@@ -8,17 +8,21 @@
 //   dV = P^T dO,  dP = dO V^T,  Dl_i = sum_d dO_id O_id,
 //   dS = P * (dP - Dl),  dQ = scale dS K,  dK = scale dS^T Q.
 // Two kernels after the row dots Dl (bwd_rowdot, shared with the CUDA-core
-// version), each over 128 x 128 tiles, bf16 operands, fp32 accumulators in
-// tensor memory:
+// version), each over whole 128 x 128 tiles, bf16 operands, fp32
+// accumulators in tensor memory:
 //   bwd_tc_dkdv: one CTA per 128-key tile of a head. It computes the
 //     transposed products S^T = K Q_i^T and dP^T = V dO_i^T, so that tensor-
-//     memory lane t (softmax thread t) owns key t: the thread rebuilds its row
-//     of P^T and dS^T over the tile's 128 queries (L and Dl of those queries
-//     staged in shared memory), writes both back as bf16 over their own
-//     columns, and the MMA accumulates dV += P^T dO_i and dK += dS^T Q_i with
-//     those as the A operand straight from tensor memory.
+//     memory lane t (rebuild thread t) owns key t: the thread rebuilds its
+//     row of P^T and dS^T over the tile's 128 queries (L and Dl of those
+//     queries staged in shared memory), writes both back as bf16 over the
+//     first half of their own columns, and the MMA accumulates dV += P^T dO_i
+//     and dK += dS^T Q_i with those as the A operand straight from tensor
+//     memory. S^T of the next query tile is issued as soon as dV has read
+//     P^T, dP^T of the next as soon as dK has read dS^T, so the rebuild of
+//     one product's operand runs under the other's MMAs.
 //   bwd_tc_dq: one CTA per 128-row query tile, the forward's orientation:
-//     S = Q K_j^T, dP = dO V_j^T, dS into tensor memory, dQ += dS K_j.
+//     S = Q K_j^T, dP = dO V_j^T, dS into tensor memory over dP, dQ += dS
+//     K_j; S of the next key tile is issued once the rebuild has read S.
 // Each output is written by one CTA, so the result is deterministic and no
 // atomics are needed; the price is that S and dP are computed twice (seven
 // products per tile pair instead of five).
@@ -41,12 +45,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 struct BwdCfg {
     // Warps [0, 4 NWG): NWG warpgroups that rebuild P and dS, each over W of
-    // a buffer's 64 columns, and write the results; then the TMA warp and the
-    // MMA warp. (Four warpgroups of 16 columns measured slower than two of 32
-    // at D = 64 as well as at D = 128.)
+    // a tile's 128 columns, and write the results; then the TMA warp and the
+    // MMA warp.
     static constexpr int NWG = 2;
-    static constexpr int W = 64 / NWG;
-    static_assert(W == 32, "the rebuild moves 32 columns per tensor-memory load");
+    static constexpr int W = kT / NWG;                   // 64 columns per warpgroup
     static constexpr int TMA_WARP = 4 * NWG, MMA_WARP = 4 * NWG + 1;
     static constexpr int THREADS = 32 * (4 * NWG + 2);
     static constexpr int PANELS = (D + 63) / 64;         // 64-column TMA boxes per tile row
@@ -60,22 +62,23 @@ struct BwdCfg {
     static constexpr int FIX_OFF = 0;                    // the CTA's resident pair (K and V, or Q and dO)
     static constexpr int RING_OFF = 2 * TILE;
     static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE;
-    static constexpr int FIX_FULL = 0, FULL = 1, EMPTY = 1 + STAGES, S_FULL = 1 + 2 * STAGES;   // S_FULL, P_FULL: one per S buffer
-    static constexpr int P_FULL = S_FULL + 2, S_READ = P_FULL + 2, DONE = S_READ + 2, DRAIN = DONE + 1;
+    static constexpr int FIX_FULL = 0, FULL = 1, EMPTY = 1 + STAGES;
+    // Once per streamed tile each: S (or S^T) and dP products landed
+    // (commits); the rebuild threads have read S, written P, read dP, written
+    // dS (NWG x 128 arrivals each).
+    static constexpr int S_FULL = 1 + 2 * STAGES, DP_FULL = S_FULL + 1, S_READ = DP_FULL + 1;
+    static constexpr int P_FULL = S_READ + 1, DP_READ = P_FULL + 1, DS_FULL = DP_READ + 1;
+    static constexpr int DONE = DS_FULL + 1, DRAIN = DONE + 1;
     static constexpr int NUM_BARS = DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
-    // Every 128-row streamed tile is handled as two 64-row halves, each with
-    // its own S and dP buffer, so that one half's rebuild of P and dS runs
-    // while the other half's products are computed. Tensor memory: S buffers
-    // (then P, bf16 pairs in their first 32 columns) at 0 and 64, dP buffers
-    // (then dS) at 128 and 192, then the accumulators (dV and dK, or dQ).
-    static constexpr int HALF_ROWS = 64;
-    static constexpr int HALF_BYTES = HALF_ROWS * 128;   // a half's row offset inside every panel
+    // Tensor memory: S (128 columns; the dK/dV kernel writes P^T, bf16
+    // pairs, over its first 64), dP (128; dS, bf16 pairs, over its first 64),
+    // then the accumulators (dV and dK, or dQ).
     static constexpr uint32_t TS = 0, TDP = 128, TACC = 256;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t ID_SS = idesc_bf16_f32(128, HALF_ROWS, false);  // 128 x 64, both K-major
-    static constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, true);     // 128 x D, B MN-major
+    static constexpr uint32_t ID_SS = idesc_bf16_f32(128, kT, false);   // 128 x 128, both K-major
+    static constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, true);    // 128 x D, B MN-major
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(TACC + 2 * D <= TMEM_COLS, "tensor memory");
 };
@@ -113,8 +116,7 @@ __device__ __forceinline__ uint32_t kstep(int kk) {
     return (kk >> 2) * (BwdCfg<D>::PANEL >> 4) + (kk & 3) * 2;
 }
 
-// D[128 x 64] = A[128 x D] B[64 x D]^T, both K-major in shared memory (B:
-// half a tile, `b` already offset to its first row).
+// D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major tiles in shared memory.
 template <int D>
 __device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a, uint32_t b) {
     const uint64_t da = desc_kmajor(a), db = desc_kmajor(b);
@@ -123,13 +125,14 @@ __device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a, uint32_
         mma_ss(d_tmem, da + kstep<D>(kk), db + kstep<D>(kk), BwdCfg<D>::ID_SS, kk > 0 ? 1u : 0u);
 }
 
-// Acc[128 x D] (+)= A[128 x 64] (bf16 pairs in tensor memory) B[64 x D]
-// (half a tile in shared memory read MN-major: its rows are the K dimension).
+// Acc[128 x D] (+)= A[128 x 128] (bf16 pairs in 64 tensor-memory columns)
+// B[128 x D] (a tile in shared memory read MN-major: its rows are the K
+// dimension).
 template <int D>
 __device__ __forceinline__ void mma_tile_acc(uint32_t acc, uint32_t a_tmem, uint32_t b, bool first) {
     const uint64_t db = desc_mnmajor<D>(b);
 #pragma unroll
-    for (int kk = 0; kk < BwdCfg<D>::HALF_ROWS / 16; ++kk)
+    for (int kk = 0; kk < kT / 16; ++kk)
         mma_ts(acc, a_tmem + kk * 8, db + kk * (2048 >> 4), BwdCfg<D>::ID_ACC, (first && kk == 0) ? 0u : 1u);
 }
 
@@ -161,74 +164,113 @@ __device__ __forceinline__ void store_acc_row(uint32_t tm_acc, bool have, bool i
     }
 }
 
-// Rebuilds W columns of this thread's row of P and dS from S and dP in
-// tensor memory: p = exp2(s * cs - L2), zero outside columns [lo, hi) of the
-// share when MASK; ds = p (dp - Dl). L2 and Dl are per column (dK/dV kernel,
-// `l2` and `dl` pointing at the share's first column, 16-byte aligned) or
-// per row (dQ kernel).
-template <int W, bool PER_COLUMN, bool MASK>
-__device__ __forceinline__ void rebuild_chunk(const uint32_t (&sr)[W], const uint32_t (&dr)[W], float cs,
-                                              const float* l2, const float* dl, float l2_row, float dl_row, int lo,
-                                              int hi, uint32_t (&pp)[W / 2], uint32_t (&dd)[W / 2]) {
+// This thread's W = 64 columns of a 128-column fp32 buffer in tensor memory.
+__device__ __forceinline__ void load_share(uint32_t taddr, uint32_t (&r)[64]) {
+    tmem_ld_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    tmem_ld_wait(r);
+}
+
+// p = exp2(s * cs - L2) over a share's 64 columns, zero outside columns
+// [lo, hi) when MASK. L2 is per column (dK/dV kernel: `l2` points at the
+// share's first query, 16-byte aligned) or per row (dQ kernel: l2_row).
+template <bool PER_COLUMN, bool MASK>
+__device__ __forceinline__ void rebuild_p(const uint32_t (&sr)[64], float cs, const float* l2, float l2_row, int lo,
+                                          int hi, float (&pv)[64]) {
 #pragma unroll
-    for (int i = 0; i < W / 4; ++i) {
-        float lv[4], dv[4];
+    for (int i = 0; i < 16; ++i) {
+        float lv[4];
         if (PER_COLUMN) {
             const float4 a = *reinterpret_cast<const float4*>(l2 + 4 * i);
-            const float4 b = *reinterpret_cast<const float4*>(dl + 4 * i);
             lv[0] = a.x, lv[1] = a.y, lv[2] = a.z, lv[3] = a.w;
-            dv[0] = b.x, dv[1] = b.y, dv[2] = b.z, dv[3] = b.w;
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) lv[e] = l2_row, dv[e] = dl_row;
+            for (int e = 0; e < 4; ++e) lv[e] = l2_row;
         }
-        float pv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int c = 4 * i + e;
-            pv[e] = ex2(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
-            if (MASK) pv[e] = (c >= lo && c < hi) ? pv[e] : 0.f;
+            const float x = ex2(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
+            pv[c] = (!MASK || (c >= lo && c < hi)) ? x : 0.f;
         }
-        pp[2 * i] = pack_bf16x2(pv[0], pv[1]);
-        pp[2 * i + 1] = pack_bf16x2(pv[2], pv[3]);
-        dd[2 * i] = pack_bf16x2(pv[0] * (__uint_as_float(dr[4 * i]) - dv[0]), pv[1] * (__uint_as_float(dr[4 * i + 1]) - dv[1]));
-        dd[2 * i + 1] =
-            pack_bf16x2(pv[2] * (__uint_as_float(dr[4 * i + 2]) - dv[2]), pv[3] * (__uint_as_float(dr[4 * i + 3]) - dv[3]));
     }
 }
 
-// One warpgroup's share of a buffer: loads its W columns of S and dP,
-// rebuilds P and dS and writes the bf16 pairs over columns [W/2 wg, W/2 (wg
-// + 1)) of the same buffers. Those columns were read by a lower warpgroup,
-// so every warpgroup signals S_READ once its loads are done and all but the
-// first wait for it before writing (the first writes inside its own
-// columns). Returns false if a wait gave up.
-template <int D, bool PER_COLUMN, bool WRITE_P>
-__device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int b, int phase, uint32_t ts, uint32_t tdp,
-                                              float cs, const float* l2, const float* dl, float l2_row, float dl_row,
-                                              int lo, int hi) {
-    using C = BwdCfg<D>;
-    constexpr int W = C::W;
-    uint32_t sr[W], dr[W], pp[W / 2], dd[W / 2];
-    tmem_ld_x32(ts + W * wg, sr);
-    tmem_ld_x32(tdp + W * wg, dr);
-    tmem_ld_wait(sr);
-    tmem_ld_wait(dr);
-    tc_fence_before();
-    mbar_arrive(c.bar(C::S_READ + b));
-    if (lo <= 0 && hi >= W)
-        rebuild_chunk<W, PER_COLUMN, false>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
-    else
-        rebuild_chunk<W, PER_COLUMN, true>(sr, dr, cs, l2, dl, l2_row, dl_row, lo, hi, pp, dd);
+// ds = p (dp - Dl) over a share's 64 columns as 32 bf16 pairs; Dl per column
+// (`dl`, 16-byte aligned) or per row (dl_row).
+template <bool PER_COLUMN>
+__device__ __forceinline__ void rebuild_ds(const float (&pv)[64], const uint32_t (&dr)[64], const float* dl,
+                                           float dl_row, uint32_t (&dd)[32]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float dv[4];
+        if (PER_COLUMN) {
+            const float4 b = *reinterpret_cast<const float4*>(dl + 4 * i);
+            dv[0] = b.x, dv[1] = b.y, dv[2] = b.z, dv[3] = b.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dv[e] = dl_row;
+        }
+        float d[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[e] = pv[4 * i + e] * (__uint_as_float(dr[4 * i + e]) - dv[e]);
+        dd[2 * i] = pack_bf16x2(d[0], d[1]);
+        dd[2 * i + 1] = pack_bf16x2(d[2], d[3]);
+    }
+}
+
+// One warpgroup's share of streamed tile k: P from S, then dS from dP. The
+// dK/dV kernel (WRITE_P) writes P^T over S's first 64 columns for the dV
+// product; both kernels write dS over dP's first 64 columns. Warpgroup wg
+// writes the 32 columns [32 wg, 32 wg + 32), which warpgroup 0 reads, so
+// every warpgroup but the first waits on the matching READ barrier before
+// writing. Returns false if a wait gave up.
+template <bool PER_COLUMN, bool WRITE_P>
+__device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int k, uint32_t ts, uint32_t tdp, float cs,
+                                              const float* l2, const float* dl, float l2_row, float dl_row, int lo,
+                                              int hi, int dp_full, int s_read, int p_full, int dp_read, int ds_full) {
+    float pv[64];
+    {
+        uint32_t sr[64];
+        load_share(ts + 64 * wg, sr);
+        tc_fence_before();
+        mbar_arrive(c.bar(s_read));
+        if (lo <= 0 && hi >= 64)
+            rebuild_p<PER_COLUMN, false>(sr, cs, l2, l2_row, lo, hi, pv);
+        else
+            rebuild_p<PER_COLUMN, true>(sr, cs, l2, l2_row, lo, hi, pv);
+    }
+    if (WRITE_P) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
+        if (wg > 0) {
+            if (!c.wait_warp(s_read, k)) return false;
+            tc_fence_after();
+        }
+        tmem_st_x32(ts + 32 * wg, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(c.bar(p_full));
+    }
+    if (!c.wait_warp(dp_full, k)) return false;
+    tc_fence_after();
+    uint32_t dd[32];
+    {
+        uint32_t dr[64];
+        load_share(tdp + 64 * wg, dr);
+        tc_fence_before();
+        mbar_arrive(c.bar(dp_read));
+        rebuild_ds<PER_COLUMN>(pv, dr, dl, dl_row, dd);
+    }
     if (wg > 0) {
-        if (!c.wait_warp(C::S_READ + b, phase)) return false;
+        if (!c.wait_warp(dp_read, k)) return false;
         tc_fence_after();
     }
-    if (WRITE_P) tmem_st_x16(ts + (W / 2) * wg, pp);
-    tmem_st_x16((WRITE_P ? tdp : ts) + (W / 2) * wg, dd);
+    tmem_st_x32(tdp + 32 * wg, dd);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(c.bar(C::P_FULL + b));
+    mbar_arrive(c.bar(ds_full));
     return true;
 }
 
@@ -242,11 +284,12 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
             mbar_init(c.bar(C::FULL + s), 1);
             mbar_init(c.bar(C::EMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(c.bar(C::S_FULL + b), 1);
-            mbar_init(c.bar(C::P_FULL + b), C::NWG * kT);
-            mbar_init(c.bar(C::S_READ + b), C::NWG * kT);
-        }
+        mbar_init(c.bar(C::S_FULL), 1);
+        mbar_init(c.bar(C::DP_FULL), 1);
+        mbar_init(c.bar(C::S_READ), C::NWG * kT);
+        mbar_init(c.bar(C::P_FULL), C::NWG * kT);
+        mbar_init(c.bar(C::DP_READ), C::NWG * kT);
+        mbar_init(c.bar(C::DS_FULL), C::NWG * kT);
         mbar_init(c.bar(C::DONE), 1);
         mbar_init(c.bar(C::DRAIN), 1);
         misc[1] = 0;
@@ -332,34 +375,32 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const uint32_t tmem = bwd_setup<D>(c, misc);
     if (warp < C::TMA_WARP) {
         // Thread t of warpgroup wg owns key key0 + t (tensor-memory lane t)
-        // and columns [W wg, W wg + W) of every 64-query half.
+        // and queries [W wg, W wg + W) of every streamed tile.
         const int wg = warp >> 2, t = threadIdx.x & 127;
         const int key = key0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const float cs = p.scale * kLog2e;
         bool ok = true;
 #pragma unroll 1
-        for (int g = 0; g < 2 * nq && ok; ++g) {
-            const int k = g >> 1, h = g & 1, b = g & 1;   // query tile, half, S/dP buffer
+        for (int k = 0; k < nq && ok; ++k) {
             const int s = k % C::STAGES;
-            const int q0 = (i0 + k) * kT + h * C::HALF_ROWS + C::W * wg;   // this share's first query
+            const int q0 = (i0 + k) * kT + C::W * wg;   // this share's first query
             // The stage's LSE2 / Dl arrived with its tiles (FULL), which the
             // MMA thread waited for before S_FULL; wait here too so that the
             // copies are visible to this thread.
-            if (!c.wait_warp(C::FULL + s, k / C::STAGES) || !c.wait_warp(C::S_FULL + b, g >> 1)) {
+            if (!c.wait_warp(C::FULL + s, k / C::STAGES) || !c.wait_warp(C::S_FULL, k)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) +
-                              h * C::HALF_ROWS + C::W * wg;
+            const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) + C::W * wg;
             const float* dl = l2 + kT;
             // Visible queries: column c with q0 + c >= key (causal); rows past
             // M have L2 = +inf; a key past N sees nothing.
             const int lo = p.causal ? key - q0 : 0;
             const int hi = key < p.N ? C::W : 0;
-            ok = rebuild_share<D, true, true>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs, l2, dl,
-                                              0.f, 0.f, lo, hi);
+            ok = rebuild_share<true, true>(c, wg, k, tm + C::TS, tm + C::TDP, cs, l2, dl, 0.f, 0.f, lo, hi, C::DP_FULL,
+                                           C::S_READ, C::P_FULL, C::DP_READ, C::DS_FULL);
         }
         if (ok && nq > 0) {
             ok = c.wait_warp(C::DONE, 0);
@@ -381,41 +422,43 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             bwd_producer<D>(c, s0, &map_k, &map_v, key0, &map_q, &map_do, i0 * kT, nq, bh, p.lse2, p.delta,
                             static_cast<int64_t>(bh) * p.Mpad + i0 * kT);
     } else if ((threadIdx.x & 31) == 0) {
-        // MMA thread. Per half query tile g: S^T = K Q^T and dP^T = V dO^T
-        // into buffer g & 1; once the softmax threads have turned them into
-        // P^T and dS^T (bf16, in place): dV += P^T dO, dK += dS^T Q. Half
-        // g + 1's products are issued before half g's gradient products, so
-        // its rebuild overlaps them; a buffer is rewritten (half g + 2) only
-        // after half g's gradient products, which read it (one thread's MMAs
-        // run in order).
+        // MMA thread. Per streamed query tile k, in this order:
+        //   dV += P^T(k) dO(k)        once the rebuild wrote P^T over S^T
+        //   S^T(k+1) = K Q(k+1)^T     S's columns are free once dV(k) read P^T
+        //   dK += dS^T(k) Q(k)        once the rebuild wrote dS^T over dP^T
+        //   dP^T(k+1) = V dO(k+1)^T   dP's columns are free once dK(k) read dS^T
+        // so the rebuild of tile k+1's P overlaps dK(k) and dP^T(k+1), and its
+        // dS overlaps dV(k+1) and S^T(k+2). One thread's MMAs run in issue
+        // order, which is what makes each overwrite safe.
         bool ok = nq > 0 && c.wait(C::FIX_FULL, 0);
         const uint32_t kt = s0 + C::FIX_OFF, vt = kt + C::TILE;
-        auto issue_sdp = [&](int g) -> bool {
-            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
-            if (h == 0 && !c.wait(C::FULL + s, k / C::STAGES)) return false;
+        auto stage = [&](int k) -> uint32_t { return s0 + C::RING_OFF + (k % C::STAGES) * C::STAGE; };
+        auto issue_s = [&](int k) -> bool {
+            if (!c.wait(C::FULL + k % C::STAGES, k / C::STAGES)) return false;
             tc_fence_after();
-            const uint32_t qt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, dot = qt + C::TILE;
-            mma_tile_nt<D>(tmem + C::TS + (g & 1) * 64, kt, qt);
-            mma_tile_nt<D>(tmem + C::TDP + (g & 1) * 64, vt, dot);
-            mma_commit(c.bar(C::S_FULL + (g & 1)));
+            mma_tile_nt<D>(tmem + C::TS, kt, stage(k));
+            mma_commit(c.bar(C::S_FULL));
             return true;
         };
-        auto issue_grad = [&](int g) -> bool {
-            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
-            if (!c.wait(C::P_FULL + (g & 1), g >> 1)) return false;
-            tc_fence_after();
-            const uint32_t qt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, dot = qt + C::TILE;
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS + (g & 1) * 64, dot, g == 0);
-            mma_tile_acc<D>(tmem + C::TACC + D, tmem + C::TDP + (g & 1) * 64, qt, g == 0);
-            if (h == 1) mma_commit(c.bar(C::EMPTY + s));
-            if (g == 2 * nq - 1) mma_commit(c.bar(C::DONE));
-            return true;
+        auto issue_dp = [&](int k) {
+            mma_tile_nt<D>(tmem + C::TDP, vt, stage(k) + C::TILE);
+            mma_commit(c.bar(C::DP_FULL));
         };
-        if (ok) ok = issue_sdp(0);
+        if (ok) ok = issue_s(0);
+        if (ok) issue_dp(0);
 #pragma unroll 1
-        for (int g = 0; ok && g < 2 * nq; ++g) {
-            if (g + 1 < 2 * nq && !issue_sdp(g + 1)) break;
-            ok = issue_grad(g);
+        for (int k = 0; ok && k < nq; ++k) {
+            const uint32_t qt = stage(k), dot = qt + C::TILE;
+            if (!c.wait(C::P_FULL, k)) break;
+            tc_fence_after();
+            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
+            if (k + 1 < nq && !issue_s(k + 1)) break;
+            if (!c.wait(C::DS_FULL, k)) break;
+            tc_fence_after();
+            mma_tile_acc<D>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
+            mma_commit(c.bar(C::EMPTY + k % C::STAGES));
+            if (k == nq - 1) mma_commit(c.bar(C::DONE));
+            if (k + 1 < nq) issue_dp(k + 1);
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
@@ -448,7 +491,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     const uint32_t tmem = bwd_setup<D>(c, misc);
     if (warp < C::TMA_WARP) {
         // Thread t of warpgroup wg owns query row r0 + t (tensor-memory lane
-        // t) and columns [W wg, W wg + W) of every 64-key half.
+        // t) and keys [W wg, W wg + W) of every streamed tile.
         const int wg = warp >> 2, t = threadIdx.x & 127;
         const int row = r0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
@@ -458,16 +501,15 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         const int lim = p.causal ? min(p.N, row + 1) : p.N;   // keys [0, lim) visible
         bool ok = true;
 #pragma unroll 1
-        for (int g = 0; g < 2 * nk && ok; ++g) {
-            const int b = g & 1;
-            if (!c.wait_warp(C::S_FULL + b, g >> 1)) {
+        for (int j = 0; j < nk && ok; ++j) {
+            if (!c.wait_warp(C::S_FULL, j)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int hi = lim - (g * C::HALF_ROWS + C::W * wg);   // this share's keys: g * 64 + W wg + column
-            ok = rebuild_share<D, false, false>(c, wg, b, g >> 1, tm + C::TS + b * 64, tm + C::TDP + b * 64, cs,
-                                                nullptr, nullptr, l2, dl, 0, hi);
+            const int hi = lim - (j * kT + C::W * wg);   // this share's keys: j * 128 + W wg + column
+            ok = rebuild_share<false, false>(c, wg, j, tm + C::TS, tm + C::TDP, cs, nullptr, nullptr, l2, dl, 0, hi,
+                                             C::DP_FULL, C::S_READ, C::P_FULL, C::DP_READ, C::DS_FULL);
         }
         if (ok && nk > 0) {
             ok = c.wait_warp(C::DONE, 0);
@@ -483,36 +525,36 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         if ((threadIdx.x & 31) == 0 && nk > 0)
             bwd_producer<D>(c, s0, &map_q, &map_do, r0, &map_k, &map_v, 0, nk, bh, nullptr, nullptr, 0);
     } else if ((threadIdx.x & 31) == 0) {
-        // MMA thread. Per half key tile g: S = Q K^T and dP = dO V^T into
-        // buffer g & 1; once the softmax threads have written dS (bf16, over
-        // S): dQ += dS K. Issue order as in the dK/dV kernel.
+        // MMA thread. Per streamed key tile j, in this order:
+        //   S(j+1) = Q K(j+1)^T   once the rebuild has read S(j)
+        //   dQ += dS(j) K(j)      once the rebuild wrote dS over dP
+        //   dP(j+1) = dO V(j+1)^T dP's columns are free once dQ(j) read dS
+        // so tile j+1's S product runs during tile j's rebuild.
         bool ok = nk > 0 && c.wait(C::FIX_FULL, 0);
         const uint32_t qt = s0 + C::FIX_OFF, dot = qt + C::TILE;
-        auto issue_sdp = [&](int g) -> bool {
-            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
-            if (h == 0 && !c.wait(C::FULL + s, k / C::STAGES)) return false;
+        auto stage = [&](int j) -> uint32_t { return s0 + C::RING_OFF + (j % C::STAGES) * C::STAGE; };
+        auto issue_s = [&](int j) -> bool {
+            if (!c.wait(C::FULL + j % C::STAGES, j / C::STAGES)) return false;
             tc_fence_after();
-            const uint32_t kt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES, vt = kt + C::TILE;
-            mma_tile_nt<D>(tmem + C::TS + (g & 1) * 64, qt, kt);
-            mma_tile_nt<D>(tmem + C::TDP + (g & 1) * 64, dot, vt);
-            mma_commit(c.bar(C::S_FULL + (g & 1)));
+            mma_tile_nt<D>(tmem + C::TS, qt, stage(j));
+            mma_commit(c.bar(C::S_FULL));
             return true;
         };
-        auto issue_grad = [&](int g) -> bool {
-            const int k = g >> 1, h = g & 1, s = k % C::STAGES;
-            if (!c.wait(C::P_FULL + (g & 1), g >> 1)) return false;
-            tc_fence_after();
-            const uint32_t kt = s0 + C::RING_OFF + s * C::STAGE + h * C::HALF_BYTES;
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS + (g & 1) * 64, kt, g == 0);
-            if (h == 1) mma_commit(c.bar(C::EMPTY + s));
-            if (g == 2 * nk - 1) mma_commit(c.bar(C::DONE));
-            return true;
+        auto issue_dp = [&](int j) {
+            mma_tile_nt<D>(tmem + C::TDP, dot, stage(j) + C::TILE);
+            mma_commit(c.bar(C::DP_FULL));
         };
-        if (ok) ok = issue_sdp(0);
+        if (ok) ok = issue_s(0);
+        if (ok) issue_dp(0);
 #pragma unroll 1
-        for (int g = 0; ok && g < 2 * nk; ++g) {
-            if (g + 1 < 2 * nk && !issue_sdp(g + 1)) break;
-            ok = issue_grad(g);
+        for (int j = 0; ok && j < nk; ++j) {
+            if (j + 1 < nk && (!c.wait(C::S_READ, j) || !issue_s(j + 1))) break;
+            if (!c.wait(C::DS_FULL, j)) break;
+            tc_fence_after();
+            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TDP, stage(j), j == 0);
+            mma_commit(c.bar(C::EMPTY + j % C::STAGES));
+            if (j == nk - 1) mma_commit(c.bar(C::DONE));
+            if (j + 1 < nk) issue_dp(j + 1);
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
