@@ -99,6 +99,57 @@ __global__ void bwd_rowdot(const BwdParams p) {
     }
 }
 
+// The same for D = 8 LR (LR = 8 or 16 lanes per row, 16-byte loads; O and dO
+// 16-byte aligned): a warp takes 32 / LR rows at a time and issues the loads
+// of four such groups before reducing any, so that enough bytes are in
+// flight to run near the HBM rate (one warp per row with 8-byte loads kept
+// too few requests outstanding: 3.0 TB/s at D = 128, 1.6 at D = 64).
+template <int LR>
+__global__ void __launch_bounds__(256) bwd_rowdot_vec(const BwdParams p) {
+    constexpr int D = 8 * LR, RPW = 32 / LR, U = 4, G = U * RPW;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LR, l = lane % LR;
+    const int64_t total = static_cast<int64_t>(p.bh_count) * p.Mpad;
+    const int64_t base = (static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32) * G;
+    uint4 ov[U], dv[U];
+    int64_t prow[U], row[U];
+    bool live[U];
+    float lse[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        prow[u] = base + u * RPW + sub;
+        const int64_t bh = prow[u] / p.Mpad;
+        const int r = static_cast<int>(prow[u] - bh * p.Mpad);
+        live[u] = prow[u] < total && r < p.M;
+        row[u] = bh * p.M + r;
+        ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
+        lse[u] = INFINITY;
+        if (live[u]) {
+            ov[u] = *reinterpret_cast<const uint4*>(p.o + row[u] * D + 8 * l);
+            dv[u] = *reinterpret_cast<const uint4*>(p.dout + row[u] * D + 8 * l);
+            if (l == 0) lse[u] = p.lse[row[u]] * kLog2e;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t ow[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
+        const uint32_t dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[i]));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[i]));
+            s = fmaf(a.x, b.x, fmaf(a.y, b.y, s));
+        }
+#pragma unroll
+        for (int off = LR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (l == 0 && prow[u] < total) {
+            p.delta[prow[u]] = live[u] ? s : 0.f;
+            p.lse2[prow[u]] = lse[u];   // +inf past M: P = 0
+        }
+    }
+}
+
 // Copies `rows` rows of width D (bf16, row-major) starting at row r0 into
 // shared memory as fp32 [kChunk][DV], zero-filling rows >= limit and
 // columns >= D.
@@ -252,6 +303,17 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t s) {
 
 cudaError_t launch_bwd_rowdot(const BwdParams& p, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(p.bh_count) * p.Mpad;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(p.o) | reinterpret_cast<uintptr_t>(p.dout)) & 15u) == 0;
+    if (aligned && (p.D == 64 || p.D == 128)) {
+        const int rows_per_block = 8 * 4 * (p.D == 64 ? 4 : 2);   // warps x groups x rows per group
+        const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        if (p.D == 64)
+            bwd_rowdot_vec<8><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+        else
+            bwd_rowdot_vec<16><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     const int64_t blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     bwd_rowdot<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
