@@ -467,11 +467,101 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
 }
 
 // --------------------------------------------------------------- dQ kernel
+// Its own layout: Q and dO resident; K and V in separate rings, since V(j)
+// is last read by dP(j) while K(j) stays until dQ(j) (with one ring of two
+// K/V stages at D = 128 the next tile's S waited for its load); dS in its
+// own tensor-memory columns, so that S(j+1) and dP(j+1) can follow as soon
+// as the rebuild has read S(j) and dP(j). The MMA thread's barrier
+// operations cost it ~100 cycles each while the tensor core streams shared
+// memory, so every barrier here serves as many waiters as it can:
+//   KFULL[s]  K(j) and V(j) landed (one barrier per K slot)
+//   SDP[v]    S(j) and dP(j) computed, V slot v free (one per V slot)
+//   KEMPTY[s] dQ(j) done: K slot s free and dS's columns free
+//   DP_READ   the rebuild has read S(j) and dP(j)
+//   DS_FULL   the rebuild has written dS(j)
+template <int D>
+struct DqCfg {
+    using B = BwdCfg<D>;
+    static constexpr int KST = (D <= 64) ? 4 : 3;        // K ring stages
+    static constexpr int VST = (D <= 64) ? 4 : 2;        // V ring stages
+    static constexpr int FIX_OFF = 0;                    // Q, dO
+    static constexpr int K_OFF = 2 * B::TILE;
+    static constexpr int V_OFF = K_OFF + KST * B::TILE;
+    static constexpr int BAR_OFF = V_OFF + VST * B::TILE;
+    static constexpr int FIX_FULL = 0, KFULL = 1, KEMPTY = KFULL + KST, SDP = KEMPTY + KST;
+    static constexpr int DP_READ = SDP + VST, DS_FULL = DP_READ + 1, DONE = DS_FULL + 1, DRAIN = DONE + 1;
+    static constexpr int NUM_BARS = DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+    // Tensor memory: S, dP (128 columns each), dS (bf16 pairs, 64), dQ (D).
+    static constexpr uint32_t TS = 0, TDP = 128, TDS = 256, TACC = 320;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(TACC + D <= B::TMEM_COLS, "tensor memory");
+};
+
+template <int D>
+__device__ __forceinline__ uint32_t dq_setup(const BwdCtx& c, uint32_t* misc) {
+    using C = DqCfg<D>;
+    if (threadIdx.x == 0) {
+        mbar_init(c.bar(C::FIX_FULL), 1);
+        for (int s = 0; s < C::KST; ++s) {
+            mbar_init(c.bar(C::KFULL + s), 1);
+            mbar_init(c.bar(C::KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) mbar_init(c.bar(C::SDP + s), 1);
+        mbar_init(c.bar(C::DP_READ), BwdCfg<D>::NWG * kT);
+        mbar_init(c.bar(C::DS_FULL), BwdCfg<D>::NWG * kT);
+        mbar_init(c.bar(C::DONE), 1);
+        mbar_init(c.bar(C::DRAIN), 1);
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x / 32 == BwdCfg<D>::MMA_WARP) {
+        tmem_alloc(smem_u32(misc), BwdCfg<D>::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return misc[0];
+}
+
+// TMA thread of the dQ kernel: Q and dO once, then K(j) and V(j) of the
+// n streamed key tiles into their rings, both signalled on K(j)'s slot.
+template <int D>
+__device__ __forceinline__ void dq_producer(const BwdCtx& c, uint32_t s0, const CUtensorMap* mq, const CUtensorMap* mdo,
+                                            int r0, const CUtensorMap* mk, const CUtensorMap* mv, int n, int bh) {
+    using C = DqCfg<D>;
+    using B = BwdCfg<D>;
+    const uint64_t pol = policy_evict_last();
+    mbar_arrive_expect_tx(c.bar(C::FIX_FULL), 2 * B::TILE);
+    load_tile<D>(s0 + C::FIX_OFF, mq, c.bar(C::FIX_FULL), r0, bh, pol);
+    load_tile<D>(s0 + C::FIX_OFF + B::TILE, mdo, c.bar(C::FIX_FULL), r0, bh, pol);
+    int kn = 0;
+#pragma unroll 1
+    for (int j = 0; j < n; ++j) {
+        const int ks = j % C::KST, vs = j % C::VST;
+        // K slot: free once dQ(j - KST) is done; V slot: once dP(j - VST) is.
+        if (j >= C::KST && !c.wait(C::KEMPTY + ks, j / C::KST - 1)) break;
+        if (j >= C::VST && !c.wait(C::SDP + vs, j / C::VST - 1)) break;
+        mbar_arrive_expect_tx(c.bar(C::KFULL + ks), 2 * B::TILE);
+        load_tile<D>(s0 + C::K_OFF + ks * B::TILE, mk, c.bar(C::KFULL + ks), j * kT, bh, pol);
+        load_tile<D>(s0 + C::V_OFF + vs * B::TILE, mv, c.bar(C::KFULL + ks), j * kT, bh, pol);
+        ++kn;
+    }
+    mbar_wait_drain(c.bar(C::FIX_FULL), 0);
+    for (int s = 0; s < C::KST && s < kn; ++s) {
+        const int last = s + ((kn - 1 - s) / C::KST) * C::KST;
+        mbar_wait_drain(c.bar(C::KFULL + s), (last / C::KST) & 1);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
           const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
-    using C = BwdCfg<D>;
+    using B = BwdCfg<D>;
+    using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(sm);
@@ -488,8 +578,8 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
     // last row.
     const int kend = p.causal ? min(p.N, min(p.M, r0 + kT)) : p.N;
     const int nk = (kend + kT - 1) / kT;
-    const uint32_t tmem = bwd_setup<D>(c, misc);
-    if (warp < C::TMA_WARP) {
+    const uint32_t tmem = dq_setup<D>(c, misc);
+    if (warp < B::TMA_WARP) {
         // Thread t of warpgroup wg owns query row r0 + t (tensor-memory lane
         // t) and keys [W wg, W wg + W) of every streamed tile.
         const int wg = warp >> 2, t = threadIdx.x & 127;
@@ -502,59 +592,77 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
         bool ok = true;
 #pragma unroll 1
         for (int j = 0; j < nk && ok; ++j) {
-            if (!c.wait_warp(C::S_FULL, j)) {
+            if (!c.wait_warp(C::SDP + j % C::VST, j / C::VST)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int hi = lim - (j * kT + C::W * wg);   // this share's keys: j * 128 + W wg + column
-            ok = rebuild_share<false, false>(c, wg, j, tm + C::TS, tm + C::TDP, cs, nullptr, nullptr, l2, dl, 0, hi,
-                                             C::DP_FULL, C::S_READ, C::P_FULL, C::DP_READ, C::DS_FULL);
+            const int hi = lim - (j * kT + B::W * wg);   // this share's keys: j * 128 + W wg + column
+            float pv[64];
+            uint32_t dd[32];
+            {
+                uint32_t sr[64], dr[64];
+                load_share(tm + C::TS + 64 * wg, sr);
+                load_share(tm + C::TDP + 64 * wg, dr);
+                tc_fence_before();
+                mbar_arrive(c.bar(C::DP_READ));
+                if (hi >= 64)
+                    rebuild_p<false, false>(sr, cs, nullptr, l2, 0, hi, pv);
+                else
+                    rebuild_p<false, true>(sr, cs, nullptr, l2, 0, hi, pv);
+                rebuild_ds<false>(pv, dr, nullptr, dl, dd);
+            }
+            // dS(j-1) must have been read by dQ(j-1) before it is overwritten.
+            if (j > 0) {
+                if (!c.wait_warp(C::KEMPTY + (j - 1) % C::KST, (j - 1) / C::KST)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            tmem_st_x32(tm + C::TDS + 32 * wg, dd);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(c.bar(C::DS_FULL));
         }
         if (ok && nk > 0) {
             ok = c.wait_warp(C::DONE, 0);
             tc_fence_after();
         }
         if (ok) {   // each warpgroup writes a share of the row's 32-column chunks
-            constexpr int kPer = (D / 32 + C::NWG - 1) / C::NWG;
+            constexpr int kPer = (D / 32 + B::NWG - 1) / B::NWG;
             const int clo = min(D / 32, wg * kPer), chi = min(D / 32, clo + kPer);
             store_acc_row<D>(tm + C::TACC, nk > 0, row < p.M, p.dq + (static_cast<int64_t>(bh) * p.M + row) * D,
                              p.scale, clo, chi);
         }
-    } else if (warp == C::TMA_WARP) {
-        if ((threadIdx.x & 31) == 0 && nk > 0)
-            bwd_producer<D>(c, s0, &map_q, &map_do, r0, &map_k, &map_v, 0, nk, bh, nullptr, nullptr, 0);
+    } else if (warp == B::TMA_WARP) {
+        if ((threadIdx.x & 31) == 0 && nk > 0) dq_producer<D>(c, s0, &map_q, &map_do, r0, &map_k, &map_v, nk, bh);
     } else if ((threadIdx.x & 31) == 0) {
         // MMA thread. Per streamed key tile j, in this order:
-        //   S(j+1) = Q K(j+1)^T   once the rebuild has read S(j)
-        //   dQ += dS(j) K(j)      once the rebuild wrote dS over dP
-        //   dP(j+1) = dO V(j+1)^T dP's columns are free once dQ(j) read dS
-        // so tile j+1's S product runs during tile j's rebuild.
+        //   S(j+1) = Q K(j+1)^T, dP(j+1) = dO V(j+1)^T   once the rebuild has
+        //                                                 read S(j) and dP(j)
+        //   dQ += dS(j) K(j)                              once it wrote dS(j)
+        // so both products of tile j+1 run during tile j's rebuild.
         bool ok = nk > 0 && c.wait(C::FIX_FULL, 0);
-        const uint32_t qt = s0 + C::FIX_OFF, dot = qt + C::TILE;
-        auto stage = [&](int j) -> uint32_t { return s0 + C::RING_OFF + (j % C::STAGES) * C::STAGE; };
-        auto issue_s = [&](int j) -> bool {
-            if (!c.wait(C::FULL + j % C::STAGES, j / C::STAGES)) return false;
+        const uint32_t qt = s0 + C::FIX_OFF, dot = qt + B::TILE;
+        auto kslot = [&](int j) -> uint32_t { return s0 + C::K_OFF + (j % C::KST) * B::TILE; };
+        auto issue_sdp = [&](int j) -> bool {
+            if (!c.wait(C::KFULL + j % C::KST, j / C::KST)) return false;
             tc_fence_after();
-            mma_tile_nt<D>(tmem + C::TS, qt, stage(j));
-            mma_commit(c.bar(C::S_FULL));
+            mma_tile_nt<D>(tmem + C::TS, qt, kslot(j));
+            mma_tile_nt<D>(tmem + C::TDP, dot, s0 + C::V_OFF + (j % C::VST) * B::TILE);
+            mma_commit(c.bar(C::SDP + j % C::VST));
             return true;
         };
-        auto issue_dp = [&](int j) {
-            mma_tile_nt<D>(tmem + C::TDP, dot, stage(j) + C::TILE);
-            mma_commit(c.bar(C::DP_FULL));
-        };
-        if (ok) ok = issue_s(0);
-        if (ok) issue_dp(0);
+        if (ok) ok = issue_sdp(0);
 #pragma unroll 1
         for (int j = 0; ok && j < nk; ++j) {
-            if (j + 1 < nk && (!c.wait(C::S_READ, j) || !issue_s(j + 1))) break;
+            if (j + 1 < nk && (!c.wait(C::DP_READ, j) || !issue_sdp(j + 1))) break;
             if (!c.wait(C::DS_FULL, j)) break;
             tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TDP, stage(j), j == 0);
-            mma_commit(c.bar(C::EMPTY + j % C::STAGES));
+            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TDS, kslot(j), j == 0);
+            mma_commit(c.bar(C::KEMPTY + j % C::KST));
             if (j == nk - 1) mma_commit(c.bar(C::DONE));
-            if (j + 1 < nk) issue_dp(j + 1);
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
@@ -571,14 +679,15 @@ cudaError_t launch_bwd_tc_t(const CUtensorMap& q, const CUtensorMap& k, const CU
     if (kv_blocks > 0x7fffffffLL || q_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     // Set on every call: the attribute belongs to the current device's context.
     cudaError_t e = cudaFuncSetAttribute(bwd_tc_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(bwd_tc_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_tc_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (kv_blocks > 0) {
         bwd_tc_dkdv<D><<<static_cast<unsigned>(kv_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    bwd_tc_dq<D><<<static_cast<unsigned>(q_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
+    bwd_tc_dq<D><<<static_cast<unsigned>(q_blocks), C::THREADS, DqCfg<D>::SMEM_BYTES, s>>>(q, k, v, dout, p);
     return cudaGetLastError();
 }
 
