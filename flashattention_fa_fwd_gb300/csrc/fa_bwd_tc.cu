@@ -62,19 +62,20 @@ struct BwdCfg {
     static constexpr int FIX_OFF = 0;                    // the CTA's resident pair (K and V, or Q and dO)
     static constexpr int RING_OFF = 2 * TILE;
     static constexpr int BAR_OFF = RING_OFF + STAGES * STAGE;
-    static constexpr int FIX_FULL = 0, FULL = 1, EMPTY = 1 + STAGES;
-    // Once per streamed tile each: S (or S^T) and dP products landed
-    // (commits); the rebuild threads have read S, written P, read dP, written
-    // dS (NWG x 128 arrivals each).
-    static constexpr int S_FULL = 1 + 2 * STAGES, DP_FULL = S_FULL + 1, S_READ = DP_FULL + 1;
-    static constexpr int P_FULL = S_READ + 1, DP_READ = P_FULL + 1, DS_FULL = DP_READ + 1;
+    // FULL[s]: stage s landed. DPE[s]: dP^T of the tile in stage s computed,
+    // which also means the previous tile's dK product is done, so that
+    // tile's stage is free (the rebuild and the producer both wait on it).
+    // S_FULL: S^T landed; P_FULL, DS_FULL: the rebuild threads wrote P^T,
+    // dS^T (NWG x 128 arrivals each).
+    static constexpr int FIX_FULL = 0, FULL = 1, DPE = 1 + STAGES;
+    static constexpr int S_FULL = 1 + 2 * STAGES, P_FULL = S_FULL + 1, DS_FULL = P_FULL + 1;
     static constexpr int DONE = DS_FULL + 1, DRAIN = DONE + 1;
     static constexpr int NUM_BARS = DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
-    // Tensor memory: S (128 columns; the dK/dV kernel writes P^T, bf16
-    // pairs, over its first 64), dP (128; dS, bf16 pairs, over its first 64),
-    // then the accumulators (dV and dK, or dQ).
+    // Tensor memory of the dK/dV kernel: S^T (128 columns; warpgroup wg
+    // writes its 64 queries of P^T, bf16 pairs, over columns [64 wg, 64 wg +
+    // 32), inside what it read itself), dP^T (likewise dS^T), then dV, dK.
     static constexpr uint32_t TS = 0, TDP = 128, TACC = 256;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t ID_SS = idesc_bf16_f32(128, kT, false);   // 128 x 128, both K-major
@@ -125,15 +126,19 @@ __device__ __forceinline__ void mma_tile_nt(uint32_t d_tmem, uint32_t a, uint32_
         mma_ss(d_tmem, da + kstep<D>(kk), db + kstep<D>(kk), BwdCfg<D>::ID_SS, kk > 0 ? 1u : 0u);
 }
 
-// Acc[128 x D] (+)= A[128 x 128] (bf16 pairs in 64 tensor-memory columns)
-// B[128 x D] (a tile in shared memory read MN-major: its rows are the K
-// dimension).
-template <int D>
+// Acc[128 x D] (+)= A[128 x 128] (bf16 pairs in tensor memory) B[128 x D]
+// (a tile in shared memory read MN-major: its rows are the K dimension). A's
+// 16-column K-steps sit at a_tmem + 8 kk (SPLIT false: 64 contiguous
+// columns) or, SPLIT, as two 32-column halves 64 columns apart (one per
+// rebuild warpgroup).
+template <int D, bool SPLIT>
 __device__ __forceinline__ void mma_tile_acc(uint32_t acc, uint32_t a_tmem, uint32_t b, bool first) {
     const uint64_t db = desc_mnmajor<D>(b);
 #pragma unroll
-    for (int kk = 0; kk < kT / 16; ++kk)
-        mma_ts(acc, a_tmem + kk * 8, db + kk * (2048 >> 4), BwdCfg<D>::ID_ACC, (first && kk == 0) ? 0u : 1u);
+    for (int kk = 0; kk < kT / 16; ++kk) {
+        const uint32_t a = SPLIT ? a_tmem + (kk >> 2) * 64 + (kk & 3) * 8 : a_tmem + kk * 8;
+        mma_ts(acc, a, db + kk * (2048 >> 4), BwdCfg<D>::ID_ACC, (first && kk == 0) ? 0u : 1u);
+    }
 }
 
 // This thread's row of a 128 x D fp32 accumulator (its tensor-memory lane),
@@ -219,58 +224,45 @@ __device__ __forceinline__ void rebuild_ds(const float (&pv)[64], const uint32_t
     }
 }
 
-// One warpgroup's share of streamed tile k: P from S, then dS from dP. The
-// dK/dV kernel (WRITE_P) writes P^T over S's first 64 columns for the dV
-// product; both kernels write dS over dP's first 64 columns. Warpgroup wg
-// writes the 32 columns [32 wg, 32 wg + 32), which warpgroup 0 reads, so
-// every warpgroup but the first waits on the matching READ barrier before
-// writing. Returns false if a wait gave up.
-template <bool PER_COLUMN, bool WRITE_P>
-__device__ __forceinline__ bool rebuild_share(const BwdCtx& c, int wg, int k, uint32_t ts, uint32_t tdp, float cs,
-                                              const float* l2, const float* dl, float l2_row, float dl_row, int lo,
-                                              int hi, int dp_full, int s_read, int p_full, int dp_read, int ds_full) {
+// One warpgroup's share of streamed tile k of the dK/dV kernel: P^T from
+// S^T, then (once dP^T(k) has landed, DPE) dS^T from dP^T, each written as
+// bf16 pairs over the first 32 of the 64 columns the warpgroup read. L2 and
+// Dl per column (`l2`, `dl`: the share's first query, 16-byte aligned).
+// Returns false if a wait gave up.
+template <int D>
+__device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uint32_t ts, uint32_t tdp, float cs,
+                                             const float* l2, const float* dl, int lo, int hi) {
+    using C = BwdCfg<D>;
     float pv[64];
     {
         uint32_t sr[64];
         load_share(ts + 64 * wg, sr);
-        tc_fence_before();
-        mbar_arrive(c.bar(s_read));
         if (lo <= 0 && hi >= 64)
-            rebuild_p<PER_COLUMN, false>(sr, cs, l2, l2_row, lo, hi, pv);
+            rebuild_p<true, false>(sr, cs, l2, 0.f, lo, hi, pv);
         else
-            rebuild_p<PER_COLUMN, true>(sr, cs, l2, l2_row, lo, hi, pv);
+            rebuild_p<true, true>(sr, cs, l2, 0.f, lo, hi, pv);
     }
-    if (WRITE_P) {
+    {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
-        if (wg > 0) {
-            if (!c.wait_warp(s_read, k)) return false;
-            tc_fence_after();
-        }
-        tmem_st_x32(ts + 32 * wg, pk);
+        tmem_st_x32(ts + 64 * wg, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(c.bar(p_full));
+        mbar_arrive(c.bar(C::P_FULL));
     }
-    if (!c.wait_warp(dp_full, k)) return false;
+    if (!c.wait_warp(C::DPE + k % C::STAGES, k / C::STAGES)) return false;
     tc_fence_after();
     uint32_t dd[32];
     {
         uint32_t dr[64];
         load_share(tdp + 64 * wg, dr);
-        tc_fence_before();
-        mbar_arrive(c.bar(dp_read));
-        rebuild_ds<PER_COLUMN>(pv, dr, dl, dl_row, dd);
+        rebuild_ds<true>(pv, dr, dl, 0.f, dd);
     }
-    if (wg > 0) {
-        if (!c.wait_warp(dp_read, k)) return false;
-        tc_fence_after();
-    }
-    tmem_st_x32(tdp + 32 * wg, dd);
+    tmem_st_x32(tdp + 64 * wg, dd);
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(c.bar(ds_full));
+    mbar_arrive(c.bar(C::DS_FULL));
     return true;
 }
 
@@ -282,13 +274,10 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
         mbar_init(c.bar(C::FIX_FULL), 1);
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(c.bar(C::FULL + s), 1);
-            mbar_init(c.bar(C::EMPTY + s), 1);
+            mbar_init(c.bar(C::DPE + s), 1);
         }
         mbar_init(c.bar(C::S_FULL), 1);
-        mbar_init(c.bar(C::DP_FULL), 1);
-        mbar_init(c.bar(C::S_READ), C::NWG * kT);
         mbar_init(c.bar(C::P_FULL), C::NWG * kT);
-        mbar_init(c.bar(C::DP_READ), C::NWG * kT);
         mbar_init(c.bar(C::DS_FULL), C::NWG * kT);
         mbar_init(c.bar(C::DONE), 1);
         mbar_init(c.bar(C::DRAIN), 1);
@@ -331,7 +320,10 @@ __device__ __forceinline__ void bwd_producer(const BwdCtx& c, uint32_t s0, const
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
         const int s = k % C::STAGES;
-        if (k >= C::STAGES && !c.wait(C::EMPTY + s, k / C::STAGES - 1)) break;
+        // Stage s last held tile k - STAGES, whose dK product is done once
+        // dP^T(k - STAGES + 1) is.
+        const int f = k - C::STAGES + 1;
+        if (k >= C::STAGES && !c.wait(C::DPE + f % C::STAGES, f / C::STAGES)) break;
         const uint32_t dst = s0 + C::RING_OFF + s * C::STAGE;
         mbar_arrive_expect_tx(c.bar(C::FULL + s), 2 * C::TILE + (lse2 ? C::VEC : 0));
         load_tile<D>(dst, r0m, c.bar(C::FULL + s), r0 + k * kT, bh, pol);
@@ -399,8 +391,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             // M have L2 = +inf; a key past N sees nothing.
             const int lo = p.causal ? key - q0 : 0;
             const int hi = key < p.N ? C::W : 0;
-            ok = rebuild_share<true, true>(c, wg, k, tm + C::TS, tm + C::TDP, cs, l2, dl, 0.f, 0.f, lo, hi, C::DP_FULL,
-                                           C::S_READ, C::P_FULL, C::DP_READ, C::DS_FULL);
+            ok = rebuild_dkdv<D>(c, wg, k, tm + C::TS, tm + C::TDP, cs, l2, dl, lo, hi);
         }
         if (ok && nq > 0) {
             ok = c.wait_warp(C::DONE, 0);
@@ -429,7 +420,8 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         //   dP^T(k+1) = V dO(k+1)^T   dP's columns are free once dK(k) read dS^T
         // so the rebuild of tile k+1's P overlaps dK(k) and dP^T(k+1), and its
         // dS overlaps dV(k+1) and S^T(k+2). One thread's MMAs run in issue
-        // order, which is what makes each overwrite safe.
+        // order, which is what makes each overwrite safe, and why DPE (the
+        // commit after dP^T(k+1)) also frees tile k's stage.
         bool ok = nq > 0 && c.wait(C::FIX_FULL, 0);
         const uint32_t kt = s0 + C::FIX_OFF, vt = kt + C::TILE;
         auto stage = [&](int k) -> uint32_t { return s0 + C::RING_OFF + (k % C::STAGES) * C::STAGE; };
@@ -442,7 +434,7 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         };
         auto issue_dp = [&](int k) {
             mma_tile_nt<D>(tmem + C::TDP, vt, stage(k) + C::TILE);
-            mma_commit(c.bar(C::DP_FULL));
+            mma_commit(c.bar(C::DPE + k % C::STAGES));
         };
         if (ok) ok = issue_s(0);
         if (ok) issue_dp(0);
@@ -451,12 +443,11 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const uint32_t qt = stage(k), dot = qt + C::TILE;
             if (!c.wait(C::P_FULL, k)) break;
             tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
+            mma_tile_acc<D, true>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
             if (k + 1 < nq && !issue_s(k + 1)) break;
             if (!c.wait(C::DS_FULL, k)) break;
             tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
-            mma_commit(c.bar(C::EMPTY + k % C::STAGES));
+            mma_tile_acc<D, true>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
             if (k == nq - 1) mma_commit(c.bar(C::DONE));
             if (k + 1 < nq) issue_dp(k + 1);
         }
@@ -660,7 +651,7 @@ bwd_tc_dq(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUt
             if (j + 1 < nk && (!c.wait(C::DP_READ, j) || !issue_sdp(j + 1))) break;
             if (!c.wait(C::DS_FULL, j)) break;
             tc_fence_after();
-            mma_tile_acc<D>(tmem + C::TACC, tmem + C::TDS, kslot(j), j == 0);
+            mma_tile_acc<D, false>(tmem + C::TACC, tmem + C::TDS, kslot(j), j == 0);
             mma_commit(c.bar(C::KEMPTY + j % C::KST));
             if (j == nk - 1) mma_commit(c.bar(C::DONE));
         }
