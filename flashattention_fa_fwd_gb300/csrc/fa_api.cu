@@ -903,6 +903,7 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
     p.D = static_cast<int>(D);
     p.scale = scale;
     p.causal = causal != 0;
+    p.sched = nullptr;
     e = fa::launch_bwd_rowdot(p, s);
     if (e == cudaSuccess && !tc) e = fa::launch_bwd(p, s);
     if (e == cudaSuccess && tc) {
@@ -914,7 +915,14 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
             mk = mq;  // never read: no key tiles exist
             mv = mq;
         }
-        e = fa::launch_bwd_tc(mq, mk, mv, mdo, p, s);
+        // The persistent dK/dV kernel claims its units from a work-counter
+        // pair, used as for the forward (the dQ kernel after it uses none).
+        if (e == cudaSuccess)
+            return with_sched_slot(s, [&](int* sched) -> fa_status {
+                p.sched = sched;
+                const cudaError_t e2 = fa::launch_bwd_tc(mq, mk, mv, mdo, p, s);
+                return e2 == cudaSuccess ? FA_OK : cuda_fail(e2, "launching the backward kernels");
+            });
     }
     if (e != cudaSuccess) return cuda_fail(e, "launching the backward kernels");
     return FA_OK;

@@ -70,9 +70,17 @@ struct BwdCfg {
     static constexpr int FIX_FULL = 0, FULL = 1, DPE = 1 + STAGES;
     static constexpr int S_FULL = 1 + 2 * STAGES, P_FULL = S_FULL + 1, DS_FULL = P_FULL + 1;
     static constexpr int DONE = DS_FULL + 1, DRAIN = DONE + 1;
-    static constexpr int NUM_BARS = DRAIN + 1;
-    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+    // The persistent dK/dV kernel: a unit's K and V no longer read
+    // (FIX_EMPTY, a commit), its dV and dK read out of tensor memory by the
+    // epilogue (ACC_FREE, NWG x 128 arrivals), and a ring of claimed units
+    // (written by the TMA thread, read by the MMA thread and every rebuild
+    // warp).
+    static constexpr int FIX_EMPTY = DRAIN + 1, ACC_FREE = FIX_EMPTY + 1;
+    static constexpr int UNIT_SLOTS = 4, UNIT_READERS = 4 * NWG + 1;
+    static constexpr int UNIT_FULL = ACC_FREE + 1, UNIT_EMPTY = UNIT_FULL + UNIT_SLOTS;
+    static constexpr int NUM_BARS = UNIT_EMPTY + UNIT_SLOTS;
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tensor-memory base, abort flag, unit ring
+    static constexpr int SMEM_BYTES = MISC_OFF + 16 + 4 * UNIT_SLOTS + 1024;
     // Tensor memory of the dK/dV kernel: S^T (128 columns; warpgroup wg
     // writes its 64 queries of P^T, bf16 pairs, over columns [64 wg, 64 wg +
     // 32), inside what it read itself), dP^T (likewise dS^T), then dV, dK.
@@ -201,6 +209,24 @@ __device__ __forceinline__ void rebuild_p(const uint32_t (&sr)[64], float cs, co
     }
 }
 
+// p = exp2(s * cs - L2) over 32 columns with per-column L2 (16-byte
+// aligned), zero outside columns [lo, hi) when MASK.
+template <bool MASK>
+__device__ __forceinline__ void rebuild_p32(const uint32_t (&sr)[32], float cs, const float* l2, int lo, int hi,
+                                            float* pv) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 a = *reinterpret_cast<const float4*>(l2 + 4 * i);
+        const float lv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = 4 * i + e;
+            const float x = ex2(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
+            pv[c] = (!MASK || (c >= lo && c < hi)) ? x : 0.f;
+        }
+    }
+}
+
 // ds = p (dp - Dl) over a share's 64 columns as 32 bf16 pairs; Dl per column
 // (`dl`, 16-byte aligned) or per row (dl_row).
 template <bool PER_COLUMN>
@@ -233,14 +259,19 @@ template <int D>
 __device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uint32_t ts, uint32_t tdp, float cs,
                                              const float* l2, const float* dl, int lo, int hi) {
     using C = BwdCfg<D>;
+    // P in two halves of 32 queries (fewer live registers); both halves are
+    // read before P^T is written over the first of them.
     float pv[64];
-    {
-        uint32_t sr[64];
-        load_share(ts + 64 * wg, sr);
-        if (lo <= 0 && hi >= 64)
-            rebuild_p<true, false>(sr, cs, l2, 0.f, lo, hi, pv);
+    const bool full = lo <= 0 && hi >= 64;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t sr[32];
+        tmem_ld_x32(ts + 64 * wg + 32 * h, sr);
+        tmem_ld_wait(sr);
+        if (full)
+            rebuild_p32<false>(sr, cs, l2 + 32 * h, lo - 32 * h, hi - 32 * h, pv + 32 * h);
         else
-            rebuild_p<true, true>(sr, cs, l2, 0.f, lo, hi, pv);
+            rebuild_p32<true>(sr, cs, l2 + 32 * h, lo - 32 * h, hi - 32 * h, pv + 32 * h);
     }
     {
         uint32_t pk[32];
@@ -253,13 +284,26 @@ __device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uin
     }
     if (!c.wait_warp(C::DPE + k % C::STAGES, k / C::STAGES)) return false;
     tc_fence_after();
-    uint32_t dd[32];
-    {
-        uint32_t dr[64];
-        load_share(tdp + 64 * wg, dr);
-        rebuild_ds<true>(pv, dr, dl, 0.f, dd);
+    // Two halves of 32 queries (fewer live registers): half h reads dP^T
+    // columns [32 h, 32 h + 32) of the share and writes its 16 columns of dS^T
+    // at [16 h, 16 h + 16), which half 0 has already read.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t dr[32], dd[16];
+        tmem_ld_x32(tdp + 64 * wg + 32 * h, dr);
+        tmem_ld_wait(dr);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 b4 = *reinterpret_cast<const float4*>(dl + 32 * h + 4 * i);
+            const float dv[4] = {b4.x, b4.y, b4.z, b4.w};
+            float q[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) q[e] = pv[32 * h + 4 * i + e] * (__uint_as_float(dr[4 * i + e]) - dv[e]);
+            dd[2 * i] = pack_bf16x2(q[0], q[1]);
+            dd[2 * i + 1] = pack_bf16x2(q[2], q[3]);
+        }
+        tmem_st_x16(tdp + 64 * wg + 16 * h, dd);
     }
-    tmem_st_x32(tdp + 64 * wg, dd);
     tmem_st_wait();
     tc_fence_before();
     mbar_arrive(c.bar(C::DS_FULL));
@@ -281,6 +325,12 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
         mbar_init(c.bar(C::DS_FULL), C::NWG * kT);
         mbar_init(c.bar(C::DONE), 1);
         mbar_init(c.bar(C::DRAIN), 1);
+        mbar_init(c.bar(C::FIX_EMPTY), 1);
+        mbar_init(c.bar(C::ACC_FREE), C::NWG * kT);
+        for (int s = 0; s < C::UNIT_SLOTS; ++s) {
+            mbar_init(c.bar(C::UNIT_FULL + s), 1);
+            mbar_init(c.bar(C::UNIT_EMPTY + s), C::UNIT_READERS);
+        }
         misc[1] = 0;
         fence_barrier_init();
     }
@@ -304,44 +354,62 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem) {
     }
 }
 
-// TMA thread: the resident pair once, then `n` streamed pairs (rows r0 +
-// 128 k), each with (when vec) the 128 padded LSE2 / Dl values at vec_row +
-// 128 k of the workspace arrays.
-template <int D>
-__device__ __forceinline__ void bwd_producer(const BwdCtx& c, uint32_t s0, const CUtensorMap* f0, const CUtensorMap* f1,
-                                             int fix_row, const CUtensorMap* r0m, const CUtensorMap* r1m, int r0, int n,
-                                             int bh, const float* lse2, const float* delta, int64_t vec_row) {
-    using C = BwdCfg<D>;
-    const uint64_t pol = policy_evict_last();
-    mbar_arrive_expect_tx(c.bar(C::FIX_FULL), 2 * C::TILE);
-    load_tile<D>(s0 + C::FIX_OFF, f0, c.bar(C::FIX_FULL), fix_row, bh, pol);
-    load_tile<D>(s0 + C::FIX_OFF + C::TILE, f1, c.bar(C::FIX_FULL), fix_row, bh, pol);
-    int issued = 0;
-#pragma unroll 1
-    for (int k = 0; k < n; ++k) {
-        const int s = k % C::STAGES;
-        // Stage s last held tile k - STAGES, whose dK product is done once
-        // dP^T(k - STAGES + 1) is.
-        const int f = k - C::STAGES + 1;
-        if (k >= C::STAGES && !c.wait(C::DPE + f % C::STAGES, f / C::STAGES)) break;
-        const uint32_t dst = s0 + C::RING_OFF + s * C::STAGE;
-        mbar_arrive_expect_tx(c.bar(C::FULL + s), 2 * C::TILE + (lse2 ? C::VEC : 0));
-        load_tile<D>(dst, r0m, c.bar(C::FULL + s), r0 + k * kT, bh, pol);
-        load_tile<D>(dst + C::TILE, r1m, c.bar(C::FULL + s), r0 + k * kT, bh, pol);
-        if (lse2) {
-            bulk_load(dst + 2 * C::TILE, lse2 + vec_row + k * kT, kT * 4, c.bar(C::FULL + s));
-            bulk_load(dst + 2 * C::TILE + kT * 4, delta + vec_row + k * kT, kT * 4, c.bar(C::FULL + s));
-        }
-        ++issued;
+// A unit of the dK/dV kernel: one 128-key tile of a head and the query
+// tiles that see it. Causal units come in groups of 8 heads, key tile 0
+// (the most query tiles) first, so that the last units to be claimed are the
+// shortest while the streamed Q and dO tiles of the heads in flight stay in
+// L2.
+struct DkdvUnit {
+    int bh, kt, nq;
+};
+
+__device__ __forceinline__ DkdvUnit dkdv_unit(int u, const BwdParams& p, int ktiles, int mtiles) {
+    DkdvUnit U;
+    if (p.causal) {
+        constexpr int kHeads = 8;
+        const int gu = kHeads * ktiles;
+        const int g = u / gu, r = u - g * gu;
+        const int hg = min(kHeads, p.bh_count - g * kHeads);
+        U.kt = r / hg;
+        U.bh = g * kHeads + r % hg;
+    } else {
+        U.bh = u / ktiles;
+        U.kt = u - U.bh * ktiles;
     }
-    mbar_wait_drain(c.bar(C::FIX_FULL), 0);
-    for (int s = 0; s < C::STAGES && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / C::STAGES) * C::STAGES;
-        mbar_wait_drain(c.bar(C::FULL + s), (last / C::STAGES) & 1);
-    }
+    const int i0 = p.causal ? U.kt : 0;   // query tiles with rows >= the tile's first key
+    U.nq = mtiles > i0 ? mtiles - i0 : 0;
+    return U;
 }
 
+// Reads the CTA's sequence of units from the ring (-1 when there are no
+// more, or a wait gave up).
+template <int D>
+struct DkdvUnitReader {
+    int k = 0;
+    __device__ __forceinline__ int next(const BwdCtx& c, const volatile int* ring, bool whole_warp) {
+        using C = BwdCfg<D>;
+        const int slot = k % C::UNIT_SLOTS, phase = k / C::UNIT_SLOTS;
+        ++k;
+        const bool ok = whole_warp ? c.wait_warp(C::UNIT_FULL + slot, phase) : c.wait(C::UNIT_FULL + slot, phase);
+        if (!ok) return -1;
+        const int u = ring[slot];
+        if (whole_warp) {
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(c.bar(C::UNIT_EMPTY + slot));
+        } else {
+            mbar_arrive(c.bar(C::UNIT_EMPTY + slot));
+        }
+        return u;
+    }
+};
+
 // ------------------------------------------------------------ dK, dV kernel
+// Persistent: one CTA per SM claims units (its own index first, then from
+// the launch's work counter). The TMA thread loads a unit's K and V once it
+// has claimed it and the previous unit's last S^T and dP^T products are done
+// (FIX_EMPTY), so that load, and the next unit's first products, overlap
+// the previous unit's last tile and its epilogue; the stage ring and every
+// per-tile barrier run on over unit boundaries.
 template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -351,69 +419,135 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(sm);
     uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::MISC_OFF);
+    volatile int* ring = reinterpret_cast<volatile int*>(misc + 4);
     BwdCtx c;
     c.bar0 = s0 + C::BAR_OFF;
     c.abort = reinterpret_cast<volatile int*>(misc + 1);
     c.err = p.err;
     const int warp = threadIdx.x / 32;
     const int ktiles = (p.N + kT - 1) / kT;
-    const int bh = static_cast<int>(blockIdx.x / ktiles);
-    const int key0 = static_cast<int>(blockIdx.x % ktiles) * kT;
     const int mtiles = p.Mpad / kT;
-    // Query tiles holding a row that sees a key of this tile: all, or
-    // (top-left causal) those with rows >= key0.
-    const int i0 = p.causal ? key0 / kT : 0;
-    const int nq = mtiles > i0 ? mtiles - i0 : 0;
+    const int units = p.bh_count * ktiles;
     const uint32_t tmem = bwd_setup<D>(c, misc);
     if (warp < C::TMA_WARP) {
         // Thread t of warpgroup wg owns key key0 + t (tensor-memory lane t)
         // and queries [W wg, W wg + W) of every streamed tile.
         const int wg = warp >> 2, t = threadIdx.x & 127;
-        const int key = key0 + t;
         const uint32_t tm = tmem + (static_cast<uint32_t>(t & ~31) << 16);
         const float cs = p.scale * kLog2e;
+        constexpr int kHalfWg = C::NWG / 2, kPer = (D / 32 + kHalfWg - 1) / kHalfWg;
+        const int part = wg % kHalfWg;
+        const int clo = min(D / 32, part * kPer), chi = min(D / 32, clo + kPer);
+        DkdvUnitReader<D> units_in;
+        int kg = 0, uc = 0;   // streamed tiles and non-empty units so far
         bool ok = true;
-#pragma unroll 1
-        for (int k = 0; k < nq && ok; ++k) {
-            const int s = k % C::STAGES;
-            const int q0 = (i0 + k) * kT + C::W * wg;   // this share's first query
-            // The stage's LSE2 / Dl arrived with its tiles (FULL), which the
-            // MMA thread waited for before S_FULL; wait here too so that the
-            // copies are visible to this thread.
-            if (!c.wait_warp(C::FULL + s, k / C::STAGES) || !c.wait_warp(C::S_FULL, k)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float* l2 = reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) + C::W * wg;
-            const float* dl = l2 + kT;
-            // Visible queries: column c with q0 + c >= key (causal); rows past
-            // M have L2 = +inf; a key past N sees nothing.
-            const int lo = p.causal ? key - q0 : 0;
-            const int hi = key < p.N ? C::W : 0;
-            ok = rebuild_dkdv<D>(c, wg, k, tm + C::TS, tm + C::TDP, cs, l2, dl, lo, hi);
-        }
-        if (ok && nq > 0) {
-            ok = c.wait_warp(C::DONE, 0);
-            tc_fence_after();
-        }
-        if (ok) {   // the first half of the warpgroups writes dV, the second dK, each a share of the chunks
+        while (ok) {
+            const int u = units_in.next(c, ring, true);
+            if (u < 0) break;
+            const DkdvUnit U = dkdv_unit(u, p, ktiles, mtiles);
+            const int key = U.kt * kT + t;
+            const int i0 = p.causal ? U.kt : 0;
             const bool in = key < p.N;
-            const int64_t off = (static_cast<int64_t>(bh) * p.N + key) * D;
-            constexpr int kHalfWg = C::NWG / 2, kPer = (D / 32 + kHalfWg - 1) / kHalfWg;
-            const int part = wg % kHalfWg;
-            const int clo = min(D / 32, part * kPer), chi = min(D / 32, clo + kPer);
-            if (wg < kHalfWg)
-                store_acc_row<D>(tm + C::TACC, nq > 0, in, p.dv + off, 1.f, clo, chi);
-            else
-                store_acc_row<D>(tm + C::TACC + D, nq > 0, in, p.dk + off, p.scale, clo, chi);
+#pragma unroll 1
+            for (int k = 0; k < U.nq && ok; ++k) {
+                const int g = kg + k, s = g % C::STAGES;
+                const int q0 = (i0 + k) * kT + C::W * wg;   // this share's first query
+                // The stage's LSE2 / Dl arrived with its tiles (FULL), which
+                // the MMA thread waited for before S_FULL; wait here too so
+                // that the copies are visible to this thread.
+                if (!c.wait_warp(C::FULL + s, g / C::STAGES) || !c.wait_warp(C::S_FULL, g)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float* l2 =
+                    reinterpret_cast<const float*>(sm + C::RING_OFF + s * C::STAGE + 2 * C::TILE) + C::W * wg;
+                const float* dl = l2 + kT;
+                // Visible queries: column c with q0 + c >= key (causal); rows
+                // past M have L2 = +inf; a key past N sees nothing.
+                const int lo = p.causal ? key - q0 : 0;
+                const int hi = in ? C::W : 0;
+                ok = rebuild_dkdv<D>(c, wg, g, tm + C::TS, tm + C::TDP, cs, l2, dl, lo, hi);
+            }
+            if (!ok) break;
+            if (U.nq > 0) {
+                if (!c.wait_warp(C::DONE, uc)) break;
+                tc_fence_after();
+            }
+            // The first half of the warpgroups writes dV, the second dK, each
+            // a share of the chunks (zeros for a key no query sees). One call
+            // site: two inlined copies kept more registers live and spilled.
+            const bool second = wg >= kHalfWg;
+            float* dst = (second ? p.dk : p.dv) + (static_cast<int64_t>(U.bh) * p.N + key) * D;
+            store_acc_row<D>(tm + C::TACC + (second ? static_cast<uint32_t>(D) : 0u), U.nq > 0, in, dst,
+                             second ? p.scale : 1.f, clo, chi);
+            if (U.nq > 0) {
+                tc_fence_before();
+                mbar_arrive(c.bar(C::ACC_FREE));
+                kg += U.nq;
+                ++uc;
+            }
         }
     } else if (warp == C::TMA_WARP) {
-        if ((threadIdx.x & 31) == 0 && nq > 0)
-            bwd_producer<D>(c, s0, &map_k, &map_v, key0, &map_q, &map_do, i0 * kT, nq, bh, p.lse2, p.delta,
-                            static_cast<int64_t>(bh) * p.Mpad + i0 * kT);
+        if ((threadIdx.x & 31) == 0) {
+            const uint64_t pol = policy_evict_last();
+            int claimed = 0;
+            auto claim = [&]() -> int {
+                const int slot = claimed % C::UNIT_SLOTS;
+                if (claimed >= C::UNIT_SLOTS && !c.wait(C::UNIT_EMPTY + slot, claimed / C::UNIT_SLOTS - 1)) return -2;
+                int v = (claimed == 0) ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
+                if (v >= units) v = -1;
+                ring[slot] = v;
+                mbar_arrive(c.bar(C::UNIT_FULL + slot));
+                ++claimed;
+                return v;
+            };
+            int sg = 0, uf = 0;   // stages issued, non-empty units loaded
+            bool ok = true;
+            int u = claim();
+            while (u >= 0 && ok) {
+                const int u_next = claim();   // one ahead: the other roles see it early
+                if (u_next == -2) break;
+                const DkdvUnit U = dkdv_unit(u, p, ktiles, mtiles);
+                if (U.nq > 0) {
+                    const int i0 = p.causal ? U.kt : 0;
+                    if (uf > 0 && !c.wait(C::FIX_EMPTY, uf - 1)) break;
+                    mbar_arrive_expect_tx(c.bar(C::FIX_FULL), 2 * C::TILE);
+                    load_tile<D>(s0 + C::FIX_OFF, &map_k, c.bar(C::FIX_FULL), U.kt * kT, U.bh, pol);
+                    load_tile<D>(s0 + C::FIX_OFF + C::TILE, &map_v, c.bar(C::FIX_FULL), U.kt * kT, U.bh, pol);
+                    const int64_t vec_row = static_cast<int64_t>(U.bh) * p.Mpad + i0 * kT;
+#pragma unroll 1
+                    for (int k = 0; k < U.nq; ++k) {
+                        const int g = sg + k, s = g % C::STAGES;
+                        // Stage s last held tile g - STAGES, whose dK product is
+                        // done once dP^T(g - STAGES + 1) is.
+                        const int f = g - C::STAGES + 1;
+                        if (g >= C::STAGES && !c.wait(C::DPE + f % C::STAGES, f / C::STAGES)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = s0 + C::RING_OFF + s * C::STAGE;
+                        mbar_arrive_expect_tx(c.bar(C::FULL + s), 2 * C::TILE + C::VEC);
+                        load_tile<D>(dst, &map_q, c.bar(C::FULL + s), (i0 + k) * kT, U.bh, pol);
+                        load_tile<D>(dst + C::TILE, &map_do, c.bar(C::FULL + s), (i0 + k) * kT, U.bh, pol);
+                        bulk_load(dst + 2 * C::TILE, p.lse2 + vec_row + k * kT, kT * 4, c.bar(C::FULL + s));
+                        bulk_load(dst + 2 * C::TILE + kT * 4, p.delta + vec_row + k * kT, kT * 4, c.bar(C::FULL + s));
+                    }
+                    if (!ok) break;
+                    sg += U.nq;
+                    ++uf;
+                }
+                u = u_next;
+            }
+            // Every copy issued must land before shared memory is released.
+            if (uf > 0) mbar_wait_drain(c.bar(C::FIX_FULL), (uf - 1) & 1);
+            for (int s = 0; s < C::STAGES && s < sg; ++s) {
+                const int last = s + ((sg - 1 - s) / C::STAGES) * C::STAGES;
+                mbar_wait_drain(c.bar(C::FULL + s), (last / C::STAGES) & 1);
+            }
+        }
     } else if ((threadIdx.x & 31) == 0) {
-        // MMA thread. Per streamed query tile k, in this order:
+        // MMA thread. Per streamed query tile k of a unit, in this order:
         //   dV += P^T(k) dO(k)        once the rebuild wrote P^T over S^T
         //   S^T(k+1) = K Q(k+1)^T     S's columns are free once dV(k) read P^T
         //   dK += dS^T(k) Q(k)        once the rebuild wrote dS^T over dP^T
@@ -421,40 +555,77 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         // so the rebuild of tile k+1's P overlaps dK(k) and dP^T(k+1), and its
         // dS overlaps dV(k+1) and S^T(k+2). One thread's MMAs run in issue
         // order, which is what makes each overwrite safe, and why DPE (the
-        // commit after dP^T(k+1)) also frees tile k's stage.
-        bool ok = nq > 0 && c.wait(C::FIX_FULL, 0);
-        const uint32_t kt = s0 + C::FIX_OFF, vt = kt + C::TILE;
-        auto stage = [&](int k) -> uint32_t { return s0 + C::RING_OFF + (k % C::STAGES) * C::STAGE; };
-        auto issue_s = [&](int k) -> bool {
-            if (!c.wait(C::FULL + k % C::STAGES, k / C::STAGES)) return false;
+        // commit after dP^T(k+1)) also frees tile k's stage. A unit's first
+        // dV overwrites the accumulators, so it waits for the previous unit's
+        // epilogue (ACC_FREE).
+        const uint32_t kt_s = s0 + C::FIX_OFF, vt_s = kt_s + C::TILE;
+        auto stage = [&](int g) -> uint32_t { return s0 + C::RING_OFF + (g % C::STAGES) * C::STAGE; };
+        auto issue_s = [&](int g) -> bool {
+            if (!c.wait(C::FULL + g % C::STAGES, g / C::STAGES)) return false;
             tc_fence_after();
-            mma_tile_nt<D>(tmem + C::TS, kt, stage(k));
+            mma_tile_nt<D>(tmem + C::TS, kt_s, stage(g));
             mma_commit(c.bar(C::S_FULL));
             return true;
         };
-        auto issue_dp = [&](int k) {
-            mma_tile_nt<D>(tmem + C::TDP, vt, stage(k) + C::TILE);
-            mma_commit(c.bar(C::DPE + k % C::STAGES));
+        auto issue_dp = [&](int g) {
+            mma_tile_nt<D>(tmem + C::TDP, vt_s, stage(g) + C::TILE);
+            mma_commit(c.bar(C::DPE + g % C::STAGES));
         };
-        if (ok) ok = issue_s(0);
-        if (ok) issue_dp(0);
+        DkdvUnitReader<D> units_in;
+        int kg = 0, uf = 0;
+        bool ok = true;
+        while (ok) {
+            const int u = units_in.next(c, ring, false);
+            if (u < 0) break;
+            const DkdvUnit U = dkdv_unit(u, p, ktiles, mtiles);
+            if (U.nq == 0) continue;
+            if (!c.wait(C::FIX_FULL, uf)) break;
+            tc_fence_after();
+            if (!issue_s(kg)) break;
+            issue_dp(kg);
+            if (U.nq == 1) mma_commit(c.bar(C::FIX_EMPTY));   // K and V read by S^T(0), dP^T(0) only
 #pragma unroll 1
-        for (int k = 0; ok && k < nq; ++k) {
-            const uint32_t qt = stage(k), dot = qt + C::TILE;
-            if (!c.wait(C::P_FULL, k)) break;
-            tc_fence_after();
-            mma_tile_acc<D, true>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
-            if (k + 1 < nq && !issue_s(k + 1)) break;
-            if (!c.wait(C::DS_FULL, k)) break;
-            tc_fence_after();
-            mma_tile_acc<D, true>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
-            if (k == nq - 1) mma_commit(c.bar(C::DONE));
-            if (k + 1 < nq) issue_dp(k + 1);
+            for (int k = 0; k < U.nq; ++k) {
+                const int g = kg + k;
+                const uint32_t qt = stage(g), dot = qt + C::TILE;
+                if (!c.wait(C::P_FULL, g) || (k == 0 && uf > 0 && !c.wait(C::ACC_FREE, uf - 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                mma_tile_acc<D, true>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
+                if (k + 1 < U.nq && !issue_s(g + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!c.wait(C::DS_FULL, g)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                mma_tile_acc<D, true>(tmem + C::TACC + D, tmem + C::TDP, qt, k == 0);
+                if (k == U.nq - 1) mma_commit(c.bar(C::DONE));
+                if (k + 1 < U.nq) {
+                    issue_dp(g + 1);
+                    if (k + 2 == U.nq) mma_commit(c.bar(C::FIX_EMPTY));   // the unit's last K, V reads
+                }
+            }
+            kg += U.nq;
+            ++uf;
         }
         mma_commit(c.bar(C::DRAIN));
         mbar_wait_drain(c.bar(C::DRAIN), 0);
     }
     bwd_teardown<D>(tmem);
+    // The last CTA to finish resets the unit counter for the next launch
+    // that uses it; every CTA's claims precede its count here.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 1, 0);
+        }
+    }
 }
 
 // --------------------------------------------------------------- dQ kernel
@@ -674,7 +845,13 @@ cudaError_t launch_bwd_tc_t(const CUtensorMap& q, const CUtensorMap& k, const CU
         e = cudaFuncSetAttribute(bwd_tc_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (kv_blocks > 0) {
-        bwd_tc_dkdv<D><<<static_cast<unsigned>(kv_blocks), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
+        if (p.sched == nullptr) return cudaErrorInvalidValue;   // the persistent kernel needs its counters
+        int dev = 0, sms = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = kv_blocks < sms ? kv_blocks : sms;   // persistent: one CTA per SM
+        bwd_tc_dkdv<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, s>>>(q, k, v, dout, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

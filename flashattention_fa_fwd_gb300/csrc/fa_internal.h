@@ -84,6 +84,8 @@ struct BwdParams {
     int D;
     float scale;
     int causal;
+    int* sched;                  // [2] work counters of the persistent dK/dV kernel
+                                 // (as Bf16Params::sched)
 };
 
 // Row dots Dl and the padded base-2 LSE (both into the workspace) on `s`.
