@@ -262,6 +262,46 @@ def test_bf16_many_launches_in_flight_on_eight_streams():
     assert not bad, f"launches {bad} differ from the serial run"
 
 
+def test_bwd_many_launches_in_flight_on_four_streams():
+    """The persistent dK/dV kernel claims its units from the same work-counter
+    slots as the forward: 80 backward calls (each with its own workspace) on
+    4 streams, enqueued without synchronisation in between, interleaved with
+    forward launches, must give exactly the gradients of a serial call.
+    Gradients start as NaN, so a unit that was skipped shows."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+    from parity import to_device_bf16
+
+    B, H, M, N, D, causal = 1, 4, 640, 640, 128, True
+    q, k, v, do = (_rand((B, H, S, D), 120 + j) for j, S in enumerate((M, N, N, M)))
+    tq, tk, tv, tdo = (to_device_bf16(x) for x in (q, k, v, do))
+    scale = D ** -0.5
+    o = torch.empty_like(tq)
+    lse = torch.empty(B, H, M, dtype=torch.float32, device="cuda")
+    fa.fa_fwd(tq, tk, tv, o, lse, scale, causal)
+    ref = [torch.empty(B, H, S, D, device="cuda") for S in (M, N, N)]
+    fa.fa_bwd(tq, tk, tv, o, lse, tdo, *ref, scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    wsb = fa.fa_bwd_workspace_bytes(B, H, M)
+    runs = [([torch.full((B, H, S, D), float("nan"), device="cuda") for S in (M, N, N)],
+             torch.empty(wsb, dtype=torch.uint8, device="cuda")) for _ in range(80)]
+    side = [(torch.empty_like(tq), torch.empty(B, H, M, device="cuda")) for _ in range(4)]
+    torch.cuda.synchronize()
+    for i, (grads, ws) in enumerate(runs):
+        with torch.cuda.stream(streams[i % 4]):
+            fa.fa_bwd(tq, tk, tv, o, lse, tdo, *grads, scale, causal, workspace=ws)
+            if i % 20 == 0:
+                fa.fa_fwd(tq, tk, tv, *side[i // 20], scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    bad = [i for i, (grads, _) in enumerate(runs) if not all(torch.equal(g, r) for g, r in zip(grads, ref))]
+    assert not bad, f"calls {bad} differ from the serial call"
+
+
 @pytest.mark.parametrize("B,H,M,N,D,causal,chunk", [(2, 5, 300, 700, 128, True, 0), (1, 7, 1000, 513, 64, False, 3),
                                                      (3, 2, 129, 0, 96, False, 4), (1, 1, 64, 200, 64, True, 1)])
 def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
