@@ -486,50 +486,33 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
             ++s_cnt;
             tc_fence_after();
             uint32_t s[128];
-            uint32_t (&s_lo)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[0]);
-            uint32_t (&s_hi)[64] = *reinterpret_cast<uint32_t(*)[64]>(&s[64]);
-            tmem_ld_x32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_ld_wait(s_lo);
-            // The second half is in flight while the first half is reduced.
-            tmem_ld_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-            tmem_ld_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+            // Row max from the tensor-memory loads themselves (tcgen05.ld.red,
+            // one maximum per 32 columns); a masked tile's maximum is taken
+            // again after masking.
+            float rr[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld_red_max_x32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q4]), rr[q4]);
+            tmem_ld_wait(s);
+            asm volatile("" : "+f"(rr[0]), "+f"(rr[1]), "+f"(rr[2]), "+f"(rr[3]));
             const int kv0 = (U.kv_lo + j) * C::BN;
             const bool need_mask = (kv0 + C::BN > p.N) || (CAUSAL && kv0 + C::BN - 1 > qt0);
-            int lim = 128;
+            float mx = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
             if (need_mask) {
-                lim = p.N - kv0;                             // key columns < N
+                int lim = p.N - kv0;                         // key columns < N
                 if (CAUSAL) lim = min(lim, qrow - kv0 + 1);  // key <= query
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
+                for (int i = 0; i < 128; ++i)
                     if (i >= lim) s[i] = __float_as_uint(-INFINITY);
-            }
-            // Row max: four independent chains of three-input maxima.
-            float mx0 = fmaxf(__uint_as_float(s[0]), __uint_as_float(s[1]));
-            float mx1 = fmaxf(__uint_as_float(s[2]), __uint_as_float(s[3]));
-            float mx2 = fmaxf(__uint_as_float(s[4]), __uint_as_float(s[5]));
-            float mx3 = fmaxf(__uint_as_float(s[6]), __uint_as_float(s[7]));
+                float mx0 = fmaxf(__uint_as_float(s[0]), __uint_as_float(s[1]));
+                float mx1 = fmaxf(__uint_as_float(s[2]), __uint_as_float(s[3]));
 #pragma unroll
-            for (int i = 8; i < 64; i += 8) {           // s[8..63]: the loaded half only
-                mx0 = fmax3(mx0, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
-                mx1 = fmax3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
-                mx2 = fmax3(mx2, __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
-                mx3 = fmax3(mx3, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+                for (int i = 4; i < 128; i += 4) {
+                    mx0 = fmax3(mx0, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+                }
+                mx = fmaxf(mx0, mx1);
             }
-            tmem_ld_wait(s_hi);
-            if (need_mask) {
-#pragma unroll
-                for (int i = 64; i < 128; ++i)
-                    if (i >= lim) s[i] = __float_as_uint(-INFINITY);
-            }
-#pragma unroll
-            for (int i = 64; i < 128; i += 8) {
-                mx0 = fmax3(mx0, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
-                mx1 = fmax3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
-                mx2 = fmax3(mx2, __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
-                mx3 = fmax3(mx3, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
-            }
-            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
             // Running max m_run: the common reference of l and acc. It moves
             // only when a tile raises the row max by more than kRescaleLog2
             // (then alpha rescales what was accumulated, as on the pages);

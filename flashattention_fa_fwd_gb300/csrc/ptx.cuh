@@ -270,6 +270,18 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+
+// Tensor-memory load of 32 columns that also returns the maximum of the
+// loaded values (per thread, i.e. per lane): sm_103a's tcgen05.ld.red.
+__device__ __forceinline__ void tmem_ld_red_max_x32(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+        : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), "=f"(mx)
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
