@@ -78,13 +78,21 @@ struct BwdCfg {
     static constexpr int FIX_EMPTY = DRAIN + 1, ACC_FREE = FIX_EMPTY + 1;
     static constexpr int UNIT_SLOTS = 4, UNIT_READERS = 4 * NWG + 1;
     static constexpr int UNIT_FULL = ACC_FREE + 1, UNIT_EMPTY = UNIT_FULL + UNIT_SLOTS;
-    static constexpr int NUM_BARS = UNIT_EMPTY + UNIT_SLOTS;
+    // OWN_P (D = 64, where tensor memory has room): P^T gets 64 columns of
+    // its own, so S^T of the next tile can follow as soon as the rebuild has
+    // read S^T (S_READ, NWG x 128 arrivals); P^T(k+1) is written once dV(k)
+    // has read P^T(k) (P_FREE, a commit).
+    static constexpr bool OWN_P = D == 64;
+    static constexpr int S_READ = UNIT_EMPTY + UNIT_SLOTS, P_FREE = S_READ + 1;
+    static constexpr int NUM_BARS = P_FREE + 1;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;   // tensor-memory base, abort flag, unit ring
     static constexpr int SMEM_BYTES = MISC_OFF + 16 + 4 * UNIT_SLOTS + 1024;
     // Tensor memory of the dK/dV kernel: S^T (128 columns; warpgroup wg
     // writes its 64 queries of P^T, bf16 pairs, over columns [64 wg, 64 wg +
-    // 32), inside what it read itself), dP^T (likewise dS^T), then dV, dK.
-    static constexpr uint32_t TS = 0, TDP = 128, TACC = 256;
+    // 32), inside what it read itself), dP^T (likewise dS^T), then dV, dK;
+    // with OWN_P, P^T sits in its own 64 columns at TP (warpgroup wg at
+    // [TP + 32 wg, TP + 32 wg + 32)) before the accumulators.
+    static constexpr uint32_t TS = 0, TDP = 128, TP = 256, TACC = OWN_P ? 320 : 256;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t ID_SS = idesc_bf16_f32(128, kT, false);   // 128 x 128, both K-major
     static constexpr uint32_t ID_ACC = idesc_bf16_f32(128, D, true);    // 128 x D, B MN-major
@@ -252,8 +260,9 @@ __device__ __forceinline__ void rebuild_ds(const float (&pv)[64], const uint32_t
 
 // One warpgroup's share of streamed tile k of the dK/dV kernel: P^T from
 // S^T, then (once dP^T(k) has landed, DPE) dS^T from dP^T, each written as
-// bf16 pairs over the first 32 of the 64 columns the warpgroup read. L2 and
-// Dl per column (`l2`, `dl`: the share's first query, 16-byte aligned).
+// bf16 pairs over the first 32 of the 64 columns the warpgroup read (P^T:
+// into its own columns with OWN_P, once dV(k-1) has read them). L2 and Dl
+// per column (`l2`, `dl`: the share's first query, 16-byte aligned).
 // Returns false if a wait gave up.
 template <int D>
 __device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uint32_t ts, uint32_t tdp, float cs,
@@ -268,6 +277,10 @@ __device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uin
         uint32_t sr[32];
         tmem_ld_x32(ts + 64 * wg + 32 * h, sr);
         tmem_ld_wait(sr);
+        if (C::OWN_P && h == 1) {   // S^T read: the next tile's S^T may follow
+            tc_fence_before();
+            mbar_arrive(c.bar(C::S_READ));
+        }
         if (full)
             rebuild_p32<false>(sr, cs, l2 + 32 * h, lo - 32 * h, hi - 32 * h, pv + 32 * h);
         else
@@ -277,7 +290,15 @@ __device__ __forceinline__ bool rebuild_dkdv(const BwdCtx& c, int wg, int k, uin
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pv[2 * i], pv[2 * i + 1]);
-        tmem_st_x32(ts + 64 * wg, pk);
+        if (C::OWN_P) {
+            if (k > 0) {
+                if (!c.wait_warp(C::P_FREE, k - 1)) return false;
+                tc_fence_after();
+            }
+            tmem_st_x32(ts + C::TP + 32 * wg, pk);
+        } else {
+            tmem_st_x32(ts + 64 * wg, pk);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(c.bar(C::P_FULL));
@@ -327,6 +348,8 @@ __device__ __forceinline__ uint32_t bwd_setup(const BwdCtx& c, uint32_t* misc) {
         mbar_init(c.bar(C::DRAIN), 1);
         mbar_init(c.bar(C::FIX_EMPTY), 1);
         mbar_init(c.bar(C::ACC_FREE), C::NWG * kT);
+        mbar_init(c.bar(C::S_READ), C::NWG * kT);
+        mbar_init(c.bar(C::P_FREE), 1);
         for (int s = 0; s < C::UNIT_SLOTS; ++s) {
             mbar_init(c.bar(C::UNIT_FULL + s), 1);
             mbar_init(c.bar(C::UNIT_EMPTY + s), C::UNIT_READERS);
@@ -588,15 +611,25 @@ bwd_tc_dkdv(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             for (int k = 0; k < U.nq; ++k) {
                 const int g = kg + k;
                 const uint32_t qt = stage(g), dot = qt + C::TILE;
+                // OWN_P: S^T(k+1) as soon as the rebuild has read S^T(k).
+                if (C::OWN_P && k + 1 < U.nq && (!c.wait(C::S_READ, g) || !issue_s(g + 1))) {
+                    ok = false;
+                    break;
+                }
                 if (!c.wait(C::P_FULL, g) || (k == 0 && uf > 0 && !c.wait(C::ACC_FREE, uf - 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                mma_tile_acc<D, true>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
-                if (k + 1 < U.nq && !issue_s(g + 1)) {
-                    ok = false;
-                    break;
+                if (C::OWN_P) {
+                    mma_tile_acc<D, false>(tmem + C::TACC, tmem + C::TP, dot, k == 0);
+                    mma_commit(c.bar(C::P_FREE));
+                } else {
+                    mma_tile_acc<D, true>(tmem + C::TACC, tmem + C::TS, dot, k == 0);
+                    if (k + 1 < U.nq && !issue_s(g + 1)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 if (!c.wait(C::DS_FULL, g)) {
                     ok = false;
