@@ -302,6 +302,44 @@ def test_bwd_many_launches_in_flight_on_four_streams():
     assert not bad, f"calls {bad} differ from the serial call"
 
 
+def test_bwd_cuda_graph_replays():
+    """fa_bwd captured once in a CUDA graph and replayed: its persistent dK/dV
+    kernel then claims units from a work-counter pair kept for captured
+    launches, which the last CTA of every replay resets. Replays with a new dO
+    copied in give exactly the gradients of a direct call."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    B, H, M, N, D, causal = 1, 3, 520, 700, 128, True
+    g = torch.Generator(device="cuda").manual_seed(11)
+    q, k, v, do = (torch.randn(B, H, S, D, device="cuda", generator=g).to(torch.bfloat16) for S in (M, N, N, M))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, M, device="cuda")
+    fa.fa_fwd(q, k, v, o, lse, D ** -0.5, causal)
+    wsb = fa.fa_bwd_workspace_bytes(B, H, M)
+    ws, ws2 = (torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(2))
+    grads = [torch.empty(B, H, S, D, device="cuda") for S in (M, N, N)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fa_bwd(q, k, v, o, lse, do, *grads, D ** -0.5, causal, workspace=ws)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fa.fa_bwd(q, k, v, o, lse, do, *grads, D ** -0.5, causal, workspace=ws)
+    for rep in range(4):
+        with torch.no_grad():
+            do.copy_(torch.randn(B, H, M, D, device="cuda", generator=g).to(torch.bfloat16))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        direct = [torch.empty_like(x) for x in grads]
+        fa.fa_bwd(q, k, v, o, lse, do, *direct, D ** -0.5, causal, workspace=ws2)
+        torch.cuda.synchronize()
+        assert all(torch.equal(x, y) for x, y in zip(grads, direct)), f"replay {rep}"
+    assert fa.fa_get_device_status() == fa.FA_OK
+
+
 @pytest.mark.parametrize("B,H,M,N,D,causal,chunk", [(2, 5, 300, 700, 128, True, 0), (1, 7, 1000, 513, 64, False, 3),
                                                      (3, 2, 129, 0, 96, False, 4), (1, 1, 64, 200, 64, True, 1)])
 def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
