@@ -65,6 +65,9 @@ def parse_args(argv=None):
                     help="time fa_fwd_splitkv with S key-range splits (0 = the library's suggestion)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size B (smaller cases for profiler captures)")
+    ap.add_argument("--seq", type=int, default=None,
+                    help="override the workload's sequence lengths M = N (studies of unit length)")
+    ap.add_argument("--noncausal", action="store_true", help="run the workload without the causal mask")
     ap.add_argument("--f32-path", choices=["ieee", "x3"], default="ieee",
                     help="fp32 workloads: exact CUDA-core fa_fwd_f32 (ieee) or tensor-core fa_fwd_f32x3 (x3)")
     ap.add_argument("--warm", action="store_true",
@@ -688,7 +691,8 @@ def gpu_arm(args, w, rank, world, local_rank):
     # The other workloads, timed after the headline in the same run (one GPU).
     per_config = None
     want = args.per_config == "on" or (args.per_config == "auto" and world == 1 and args.workload == DEFAULT_WORKLOAD
-                                         and args.batch is None and not bwd and splits == 1)
+                                         and args.batch is None and args.seq is None and not args.noncausal
+                                         and not bwd and splits == 1)
     if want:
         del hq, hk, hv, ho, hl
         e2e_step = ws_host = None   # drops the e2e step's device buffers
@@ -776,10 +780,14 @@ def main(argv=None):
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     w = WORKLOADS[args.workload]
-    if args.batch is not None:
-        import dataclasses
+    import dataclasses
 
+    if args.batch is not None:
         w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_batch{args.batch}")
+    if args.seq is not None:
+        w = dataclasses.replace(w, M=args.seq, N=args.seq, name=f"{w.name}_seq{args.seq}")
+    if args.noncausal:
+        w = dataclasses.replace(w, causal=False, name=f"{w.name}_noncausal")
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
