@@ -44,9 +44,9 @@
  * which it keeps until the process exits: a status word, into which
  * device-side failures (a pipeline wait that ran out of time) are OR-ed and
  * which fa_get_device_status() reads, and 128 pairs of work counters that
- * the bf16 kernel's CTAs use to claim work units. Each bf16 launch (fa_fwd,
- * fa_fwd_splitkv, fa_fwd_host) takes the next of 64 pairs in turn and leaves
- * it at zero when it ends; before reusing a pair, the launch's stream waits
+ * the persistent kernels' CTAs use to claim work units. Each bf16 forward
+ * launch (fa_fwd, fa_fwd_splitkv, fa_fwd_host) and each tensor-core fa_bwd
+ * call takes the next of 64 pairs in turn and leaves it at zero when it ends; before reusing a pair, the launch's stream waits
  * for an event recorded after the pair's previous launch, so any number of
  * launches may be in flight on any streams and host threads without two
  * running launches sharing a pair (the 65th queues behind the first). A
@@ -280,12 +280,13 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
  * of P is rebuilt as exp(S - L) from Q, K and the forward's per-row
  * log-sum-exp L (`lse`). With that P: dV = P^T dO, dP = dO V^T,
  * dS = P * (dP - rowsum(dO * O)), dQ = scale dS K, dK = scale dS^T Q.
- * D in {64, 96, 128} runs on the tensor cores (tcgen05, TMA): one kernel
- * per 128-key tile computes S^T = K Q^T and dP^T = V dO^T, rebuilds P^T and
- * dS^T (bf16) in tensor memory and accumulates dV, dK there; one per
- * 128-row query tile does the same for dQ. Other D run on the CUDA cores in
- * fp32. Both are deterministic (each output written by one CTA, no
- * atomics).
+ * D in {64, 96, 128} runs on the tensor cores (tcgen05, TMA): a persistent
+ * kernel whose CTAs take 128-key tiles in turn computes S^T = K Q^T and
+ * dP^T = V dO^T, rebuilds P^T and dS^T (bf16) in tensor memory and
+ * accumulates dV, dK there (its CTAs claim tiles from one of the work-counter
+ * pairs described above); one kernel per 128-row query tile does the same
+ * for dQ. Other D run on the CUDA cores in fp32. Both are deterministic (each
+ * output written by one CTA, no atomics).
  *
  *   q, k, v          the forward's bf16 inputs, [B,H,M,D] / [B,H,N,D]
  *   o, lse           the forward's outputs for them (bf16 O, fp32 LSE)
