@@ -160,6 +160,13 @@ fa_status with_sched_slot(cudaStream_t s, Launch&& launch) {
     return FA_OK;
 }
 
+// Causal units are claimed longest first inside groups of this many heads:
+// small enough that the groups in flight keep their K and V in L2, large
+// enough that the last group has many more units than CTAs, so the short
+// units balance the end of the launch (8-head groups left CTAs idle for 4 %
+// of a causal 4K launch at D = 128; 16 measured +2.1 %).
+constexpr int64_t kCausalHeadsPerGroup = 16;
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
@@ -269,7 +276,7 @@ fa_status launch_fwd_checked(const void* q, const void* k, const void* v, void* 
     p.num_units = static_cast<int>(bh * n_pairs);
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
-    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.heads_per_group = static_cast<int>(bh < kCausalHeadsPerGroup ? bh : kCausalHeadsPerGroup);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     return with_sched_slot(s, [&](int* sched) -> fa_status {
         p.sched = sched;
@@ -486,7 +493,7 @@ FA_API fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, voi
     p.num_units = static_cast<int>(bh * n_pairs * num_splits);
     p.ws_o = static_cast<float*>(workspace);
     p.ws_lse = p.ws_o + num_splits * bh * M * D;
-    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.heads_per_group = static_cast<int>(bh < kCausalHeadsPerGroup ? bh : kCausalHeadsPerGroup);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = with_sched_slot(s, [&](int* sched) -> fa_status {
@@ -622,7 +629,7 @@ FA_API fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, voi
     p.num_units = static_cast<int>(bh * n_pairs);
     p.ws_o = nullptr;
     p.ws_lse = nullptr;
-    p.heads_per_group = static_cast<int>(bh < 8 ? bh : 8);
+    p.heads_per_group = static_cast<int>(bh < kCausalHeadsPerGroup ? bh : kCausalHeadsPerGroup);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     p.sched = reinterpret_cast<int*>(scratch + 1);
     switch (D) {

@@ -25,7 +25,7 @@ struct Bf16Params {
     int num_units;       // bh_count * n_pairs * splits
     float* ws_o;         // splits > 1: [splits, BH, M, D] fp32 partial outputs
     float* ws_lse;       // splits > 1: [splits, BH, M] fp32 partial log-sum-exps
-    int heads_per_group; // causal tile order: heads that share a group
+    int heads_per_group; // causal unit order: heads that share a group (longest units first within it)
     float scale_log2;    // scale * log2(e)
     int* sched;          // [2]: next unit to claim, CTAs finished. Zero when the
                          // launch starts; the launch's last CTA sets both back
