@@ -111,7 +111,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * multiply-adds (no TF32): the single-head fp32 problem of "FlashAttention
  * in Triton: A Tile-by-Tile Walkthrough" (its kernel computes its dots in
  * IEEE fp32), generalised to [B, H] and the causal mask. All buffers fp32.
- * D must be in [1, 128].
+ * D must be in [1, 128]. Problems with few rows also cut the keys across
+ * the CTAs of a thread-block cluster and merge the partial results with the
+ * softmax-of-a-concatenation rule of "Module 08: FlashAttention and
+ * Memory-Efficient Kernels" (section "Tiling and the online softmax"), in a
+ * fixed order: results are deterministic. One kernel launch, no workspace.
  */
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                      int64_t B, int64_t H, int64_t M, int64_t N, int64_t D,

@@ -56,6 +56,25 @@ def test_f32_odd_sizes(M, N, D, causal):
     check_f32(o, lse, o_ref, lse_ref, f"f32 {M}x{N}x{D} causal={causal}")
 
 
+@pytest.mark.parametrize("B,H,M,N,D,causal", [
+    (1, 1, 256, 512, 64, True),      # 8 CTAs per cluster, 2 key tiles each
+    (1, 2, 100, 1000, 96, False),    # 8, 4 tiles each, D padded to 128
+    (2, 1, 8, 4096, 128, False),     # 8, 16 tiles each: the double-buffered loop
+    (2, 1, 8, 4096, 128, True),
+    (1, 1, 1, 33, 64, False),        # 2, the second holding key 32 alone
+    (1, 3, 300, 200, 17, True),      # 4, the last split one ragged tile
+    (1, 1, 40, 1000, 64, True),      # 8, most splits beyond every row's keys
+])
+def test_f32_key_split_shapes(B, H, M, N, D, causal):
+    """Problems with too few rows to fill the GPU: the fp32 path cuts the
+    keys across a thread-block cluster and merges the partial (acc, m, l)
+    of each row (the comment gives the cluster size the library picks)."""
+    q, k, v = (_rand((B, H, r, D), 7 * M + N + D + i, bf16=False) for i, r in enumerate((M, N, N)))
+    o, lse = run_f32(q, k, v, 1 / math.sqrt(D), causal)
+    o_ref, lse_ref = attention(q, k, v, 1 / math.sqrt(D), causal)
+    check_f32(o, lse, o_ref, lse_ref, f"f32 key split {B}x{H}x{M}x{N}x{D} causal={causal}")
+
+
 def test_f32_worked_example():
     """Scores [1, 2, 3], values [10, 20, 30] ("FlashAttention in Triton",
     worked example): output 25.752 to the page's three decimals."""
