@@ -166,7 +166,9 @@ __device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
         U.bh = u / p.n_pairs;
         pair = u - U.bh * p.n_pairs;
     }
-    U.q0 = pair * 256;
+    // A unit is a pair of 128-row query tiles, or one tile (tile 1 unused)
+    // when the launch runs in single-tile units.
+    U.q0 = pair * (p.single ? 128 : 256);
     const int nkv = (p.N + 127) / 128;
     // This split's key tiles are [kv_lo, kv_hi).
     const int per = (nkv + p.splits - 1) / p.splits;
@@ -177,7 +179,7 @@ __device__ __forceinline__ Unit unit_info(int u, const Bf16Params& p) {
     const int lim0 = CAUSAL ? min(kv_hi, U.q0 / 128 + 1) : kv_hi;
     const int lim1 = CAUSAL ? min(kv_hi, (U.q0 + 128) / 128 + 1) : kv_hi;
     U.n0 = (U.q0 >= p.M) ? 0 : max(0, lim0 - U.kv_lo);
-    U.n1 = (U.q0 + 128 >= p.M) ? 0 : max(0, lim1 - U.kv_lo);
+    U.n1 = (p.single || U.q0 + 128 >= p.M) ? 0 : max(0, lim1 - U.kv_lo);
     U.nmax = max(U.n0, U.n1);
     return U;
 }
@@ -647,7 +649,8 @@ __device__ __forceinline__ void epilogue_role(const Bf16Params& p, const Ctx& c)
         for (int t = 0; t < 2; ++t) {
             const int nt = t ? U.n1 : U.n0;
             const int qt0 = U.q0 + 128 * t;
-            if (!ok || qt0 >= p.M) continue;
+            // Tile 1 of a single-tile unit is another unit's query tile.
+            if (!ok || qt0 >= p.M || (t == 1 && p.single)) continue;
             float m_fin = -INFINITY, l_fin = 0.f, lo_fin = 0.f;
             if (nt > 0) {
                 bool w = c.wait_warp(C::ST_FULL + t, st_cnt[t]);

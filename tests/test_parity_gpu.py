@@ -387,6 +387,34 @@ def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
     assert torch.equal(o, do.cpu()) and torch.equal(lse, dl.cpu())
 
 
+@pytest.mark.parametrize("D", [96, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_unit_shape_does_not_change_results(D, causal):
+    """Problems with fewer query-tile pairs than SMs run in units of one
+    query tile, larger ones in pairs; a head computed either way gives the
+    same bits, and matches the oracle."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    M, N, heads = 600, 700, 64        # 3 pairs (5 tiles, the last ragged) per head; 192 pairs in all
+    g = torch.Generator().manual_seed(D * 10 + int(causal))
+    q, k, v = (torch.randn(1, heads, r, D, generator=g).to(torch.bfloat16).cuda() for r in (M, N, N))
+    o_all = torch.empty_like(q)
+    l_all = torch.empty(1, heads, M, device="cuda")
+    fa.fa_fwd(q, k, v, o_all, l_all, D ** -0.5, causal)                   # pairs of query tiles
+    q2, k2, v2 = (x[:, :2].contiguous() for x in (q, k, v))
+    o_two = torch.empty_like(q2)
+    l_two = torch.empty(1, 2, M, device="cuda")
+    fa.fa_fwd(q2, k2, v2, o_two, l_two, D ** -0.5, causal)                # 6 pairs: single query tiles
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert torch.equal(o_two, o_all[:, :2]) and torch.equal(l_two, l_all[:, :2])
+    qn, kn, vn = (x.float().cpu().numpy() for x in (q2, k2, v2))
+    o_ref, lse_ref = attention(qn, kn, vn, D ** -0.5, causal)
+    check_bf16(o_two.float().cpu().numpy(), l_two.cpu().numpy(), o_ref, lse_ref, f"unit shape D={D} causal={causal}")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """Failure detection without a fault: a kernel waits, with the kernels'
     bounded barrier wait, on a phase nothing completes. After 20 ms it gives
