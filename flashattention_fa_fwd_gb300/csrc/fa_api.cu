@@ -247,18 +247,20 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
 namespace {
 
 // Work units of the two-tile kernel without key splits: pairs of 128-row
-// query tiles, or single tiles when the pairs would leave SMs idle (the
-// cross-attention workload has 64 pairs and 128 tiles for 152 SMs: single
-// tiles measured +7 %). A row's arithmetic is the same either way, so the
-// choice never changes a result. At D = 64 the one-tile kernel runs and
-// sets its own units.
+// query tiles, or single tiles when every tile fits on its own SM. A CTA
+// steps one tile through the keys in ~3/4 of the time it takes for a pair,
+// so single tiles win while they need one wave and pairs would leave SMs
+// idle (the cross-attention workload: 64 pairs, 128 tiles, 152 SMs; +7 %),
+// and lose once they need two. A row's arithmetic is the same either way,
+// so the choice never changes a result. At D = 64 the one-tile kernel runs
+// and sets its own units.
 void set_units(fa::Bf16Params& p, int64_t bh, int64_t M) {
-    const int64_t pairs = (M + 255) / 256;
+    const int64_t pairs = (M + 255) / 256, tiles = (M + 127) / 128;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    p.single = (bh * pairs < sms) ? 1 : 0;
-    p.n_pairs = static_cast<int>(p.single ? (M + 127) / 128 : pairs);
+    p.single = (tiles > pairs && bh * tiles <= sms) ? 1 : 0;
+    p.n_pairs = static_cast<int>(p.single ? tiles : pairs);
     p.splits = 1;
     p.num_units = static_cast<int>(bh * p.n_pairs);
 }

@@ -22,9 +22,9 @@ struct Bf16Params {
     int N;
     int n_pairs;         // query-tile units per head: ceil(M / 256) pairs of 128-row
                          // tiles, or ceil(M / 128) single tiles when `single`
-    int single;          // 1: units of one query tile (tile 1 idle), for problems
-                         // whose pairs would leave SMs idle; a row's arithmetic
-                         // is the same either way
+    int single;          // 1: units of one query tile (tile 1 idle), when every
+                         // tile fits on its own SM; a row's arithmetic is the
+                         // same either way
     int splits;          // key-range splits per unit (1 = no split)
     int num_units;       // bh_count * n_pairs * splits
     float* ws_o;         // splits > 1: [splits, BH, M, D] fp32 partial outputs

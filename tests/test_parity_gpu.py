@@ -390,14 +390,14 @@ def test_host_entry_matches_device_entry(B, H, M, N, D, causal, chunk):
 @pytest.mark.parametrize("D", [96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_unit_shape_does_not_change_results(D, causal):
-    """Problems with fewer query-tile pairs than SMs run in units of one
-    query tile, larger ones in pairs; a head computed either way gives the
-    same bits, and matches the oracle."""
+    """Problems whose 128-row query tiles all fit on their own SMs run in
+    units of one query tile, larger ones in pairs of tiles; a head computed
+    either way gives the same bits, and matches the oracle."""
     import torch
 
     import flashattention_fa_fwd_gb300 as fa
 
-    M, N, heads = 600, 700, 64        # 3 pairs (5 tiles, the last ragged) per head; 192 pairs in all
+    M, N, heads = 600, 700, 64        # 5 query tiles per head, the last ragged: 320 in all, 10 for two heads
     g = torch.Generator().manual_seed(D * 10 + int(causal))
     q, k, v = (torch.randn(1, heads, r, D, generator=g).to(torch.bfloat16).cuda() for r in (M, N, N))
     o_all = torch.empty_like(q)
@@ -406,7 +406,7 @@ def test_bf16_unit_shape_does_not_change_results(D, causal):
     q2, k2, v2 = (x[:, :2].contiguous() for x in (q, k, v))
     o_two = torch.empty_like(q2)
     l_two = torch.empty(1, 2, M, device="cuda")
-    fa.fa_fwd(q2, k2, v2, o_two, l_two, D ** -0.5, causal)                # 6 pairs: single query tiles
+    fa.fa_fwd(q2, k2, v2, o_two, l_two, D ** -0.5, causal)                # single query tiles
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == fa.FA_OK
     assert torch.equal(o_two, o_all[:, :2]) and torch.equal(l_two, l_all[:, :2])
