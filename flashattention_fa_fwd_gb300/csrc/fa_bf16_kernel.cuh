@@ -12,7 +12,9 @@
 // scale so that each score costs one FMA and one base-two exponential. The per-row log-sum-exp
 // m + log(l) is written next to O ("Module 08", section "The backward pass").
 //
-// Work unit: one (batch*head, pair of 128-row query tiles). Each CTA is
+// Work unit: one (batch*head, pair of 128-row query tiles), or one query
+// tile when every tile of the problem fits on its own SM (Bf16Params::single;
+// tile 1 then stays idle). Each CTA is
 // persistent (one per SM) and claims units one at a time from a global
 // counter, in an order that puts the longest causal units of a group of
 // heads first (unit_info), so that CTAs finish within one short unit of each
