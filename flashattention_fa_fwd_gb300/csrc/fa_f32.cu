@@ -21,6 +21,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -451,8 +452,28 @@ fa_fwd_f32_split(const F32Params p, bool causal, int tiles_per_split) {
     cluster.sync();   // no CTA leaves while another still reads its partials
 }
 
+// The current device's ordinal and SM count (0 SMs if they cannot be read).
+int device_sms(int* dev_out) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    *dev_out = dev;
+    return n;
+}
+
+// Whether a cluster of `splits` CTAs of the key-split kernel can be resident
+// on the device at all (a partitioned GPU may offer fewer SMs per cluster);
+// asked once per device, head-dimension class and cluster size. When it
+// cannot, the warp-per-row kernel runs instead.
+constexpr int kMaxDev = 64;
+std::atomic<int> g_cluster_ok[kMaxDev][3][4];   // 0 unknown, 1 yes, -1 no
+
+// Launches the key-split kernel; sets *launched to false, launching nothing,
+// when its clusters cannot be scheduled on this device.
 template <int DMAX>
-cudaError_t launch_split_t(const F32Params& p, bool causal, int splits, int tiles_per_split, cudaStream_t s) {
+cudaError_t launch_split_t(const F32Params& p, bool causal, int splits, int tiles_per_split, cudaStream_t s,
+                           int dev, bool* launched) {
+    *launched = false;
     const int smem = (4 * kKeys * (DMAX + 4) + kSplitRows * DMAX + kSplitRows * (DMAX + 2)) * static_cast<int>(sizeof(float));
     auto kern = fa_fwd_f32_split<DMAX>;
     if (smem > 48 * 1024) {
@@ -472,6 +493,18 @@ cudaError_t launch_split_t(const F32Params& p, bool causal, int splits, int tile
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const int di = DMAX == 32 ? 0 : (DMAX == 64 ? 1 : 2), si = splits == 2 ? 0 : (splits == 4 ? 1 : 2);
+    std::atomic<int>* ok = (dev >= 0 && dev < kMaxDev) ? &g_cluster_ok[dev][di][si] : nullptr;
+    int known = ok ? ok->load(std::memory_order_relaxed) : 0;
+    if (known == 0) {
+        int clusters = 0;
+        const cudaError_t oe = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (oe != cudaSuccess) (void)cudaGetLastError();   // not a launch: nothing to report
+        known = (oe == cudaSuccess && clusters > 0) ? 1 : -1;
+        if (ok) ok->store(known, std::memory_order_relaxed);
+    }
+    if (known < 0) return cudaSuccess;
+    *launched = true;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p, causal, tiles_per_split);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -481,11 +514,11 @@ cudaError_t launch_split_t(const F32Params& p, bool causal, int splits, int tile
 // The key-split cluster count for a problem: doubled (up to the portable
 // cluster size) while the CTAs stay under two per SM and every split keeps
 // at least one 32-key tile; 1 means no split.
-int f32_key_splits(long long bh_count, long long M, long long N) {
+int f32_key_splits(long long bh_count, long long M, long long N, int sms) {
     const long long groups = (M + kSplitRows - 1) / kSplitRows * bh_count;
     const long long tiles = (N + kKeys - 1) / kKeys;
     int splits = 1;
-    while (splits < kMaxSplits && groups * splits < 2 * 152 && 2 * splits <= tiles) splits *= 2;
+    while (splits < kMaxSplits && groups * splits < 2LL * sms && 2 * splits <= tiles) splits *= 2;
     return splits;
 }
 
@@ -495,14 +528,20 @@ int f32_key_splits(long long bh_count, long long M, long long N) {
 // also cut across a cluster when the rows' warps alone fill less than two
 // CTAs per SM.
 cudaError_t launch_f32(const F32Params& p, bool causal, cudaStream_t s) {
-    const bool many = static_cast<long long>(p.bh_count) * p.M >= 152LL * 4 * kRows;
-    const int splits = many ? 1 : f32_key_splits(p.bh_count, p.M, p.N);
+    int dev = -1;
+    int sms = device_sms(&dev);
+    if (sms <= 0) sms = 152;
+    const bool many = static_cast<long long>(p.bh_count) * p.M >= static_cast<long long>(sms) * 4 * kRows;
+    const int splits = many ? 1 : f32_key_splits(p.bh_count, p.M, p.N, sms);
     if (splits > 1) {
         const int tiles = (p.N + kKeys - 1) / kKeys;
         const int per = (tiles + splits - 1) / splits;
-        if (p.D <= 32) return launch_split_t<32>(p, causal, splits, per, s);
-        if (p.D <= 64) return launch_split_t<64>(p, causal, splits, per, s);
-        return launch_split_t<128>(p, causal, splits, per, s);
+        bool launched = false;
+        cudaError_t e;
+        if (p.D <= 32) e = launch_split_t<32>(p, causal, splits, per, s, dev, &launched);
+        else if (p.D <= 64) e = launch_split_t<64>(p, causal, splits, per, s, dev, &launched);
+        else e = launch_split_t<128>(p, causal, splits, per, s, dev, &launched);
+        if (e != cudaSuccess || launched) return e;
     }
     if (p.D <= 32) return many ? launch_rows_t<32>(p, causal, s) : launch_warps_t<32>(p, causal, s);
     if (p.D <= 64) return many ? launch_rows_t<64>(p, causal, s) : launch_warps_t<64>(p, causal, s);
