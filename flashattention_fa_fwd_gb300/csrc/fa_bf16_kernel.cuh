@@ -429,6 +429,14 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
                     mma_commit(c.bar(C::O_DONE + 1));
                     ++uo1;
                 }
+            } else if (j >= 1 && n1 == 0 && !p.single) {
+                // Tile 1 lies beyond M: its softmax's empty hand-off keeps
+                // it in step (tile1_lockstep).
+                if (!c.wait(C::P_FULL + 1, pv1)) {
+                    ok = false;
+                    break;
+                }
+                ++pv1;
             }
             if (j < n1) {
                 tc_fence_after();
@@ -449,6 +457,26 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& c) {
 }
 
 // ---------------------------------------------------------------- softmax
+// Tile 1's softmax for a pair whose tile 1 lies beyond M: it steps with the
+// MMA thread anyway, waiting for each of the unit's `n` steps and handing
+// over an empty P, so that it is never more than two steps ahead of the
+// MMA thread. The ITER ring is waited on by phase parity, which only tells
+// phase k from k + 1; skipping the unit's steps could put tile 1 ITERS or
+// more steps ahead, where a phase not yet begun reads as complete. Kept out
+// of line so that the softmax's own loop keeps its registers.
+template <int ITERS>
+__device__ __noinline__ bool tile1_lockstep(uint32_t iter0, uint32_t p_full1, volatile int* abort, uint32_t* err,
+                                            int itb, int n) {
+    for (int j = 0; j < n; ++j) {
+        const int s = itb + j;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(iter0 + 8u * static_cast<uint32_t>(s % ITERS),
+                                                          static_cast<uint32_t>(s / ITERS) & 1u, abort, err));
+        if (!ok) return false;
+        mbar_arrive(p_full1);
+    }
+    return true;
+}
+
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const Ctx& c) {
     using C = Bf16Cfg<D>;
@@ -470,6 +498,10 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
         const int itb = it_base;
         if (U.nmax > 0) it_base += U.nmax + 1;
         const int ntile = t ? U.n1 : U.n0;
+        if (t == 1 && ntile == 0 && U.nmax > 0 && !p.single) {
+            ok = tile1_lockstep<C::ITERS>(c.bar(C::ITER), c.bar(C::P_FULL + 1), c.abort, c.err, itb, U.nmax);
+            continue;
+        }
         if (ntile == 0) continue;
         const int qt0 = U.q0 + 128 * t;                     // first row of the tile
         const int qrow = qt0 + r;
@@ -480,7 +512,8 @@ __device__ __forceinline__ void softmax_role(int t, const Bf16Params& p, const C
             // Every lane must agree: the tensor-memory loads below are
             // warp-collective.
             // S_0(j) has its own barrier; S_1(j) is announced by step j's
-            // ITER commit.
+            // ITER commit (sound while tile 1 stays within ITERS - 1 steps of
+            // the MMA thread, which the lockstep below guarantees).
             const bool s_ok = t == 0 ? c.wait_warp(C::S_FULL, s_cnt)
                                      : c.wait_warp(C::ITER + (itb + j) % C::ITERS, (itb + j) / C::ITERS);
             if (!s_ok) {

@@ -415,6 +415,44 @@ def test_bf16_unit_shape_does_not_change_results(D, causal):
     check_bf16(o_two.float().cpu().numpy(), l_two.cpu().numpy(), o_ref, lse_ref, f"unit shape D={D} causal={causal}")
 
 
+@pytest.mark.parametrize("M,N,heads,causal", [(300, 2048, 400, False), (1100, 1100, 100, True)])
+def test_bf16_pairs_after_units_without_tile1(M, N, heads, causal):
+    """An odd number of 128-row query tiles leaves each head's last pair
+    without a second tile, and with many heads every CTA runs several such
+    units among full pairs: tile 1's softmax then skips 10 to 17 MMA steps
+    at a time. Every head must come out as it does in small launches of a
+    few heads (units of one query tile), bit for bit, and sampled heads must
+    match the oracle."""
+    import torch
+
+    import flashattention_fa_fwd_gb300 as fa
+
+    D = 128
+    g = torch.Generator(device="cuda").manual_seed(M + N + heads)
+    q, k, v = (torch.randn(1, heads, r, D, device="cuda", generator=g).to(torch.bfloat16) for r in (M, N, N))
+    o = torch.empty_like(q)
+    lse = torch.empty(1, heads, M, device="cuda")
+    fa.fa_fwd(q, k, v, o, lse, D ** -0.5, causal)
+    chunk = 10                                          # 10 heads: at most 90 query tiles, single-tile units
+    o_c, lse_c = torch.empty_like(o), torch.empty_like(lse)
+    for h0 in range(0, heads, chunk):
+        sl = slice(h0, h0 + chunk)
+        qc, kc, vc = (x[:, sl].contiguous() for x in (q, k, v))
+        oc = torch.empty_like(qc)
+        lc = torch.empty(1, qc.shape[1], M, device="cuda")
+        fa.fa_fwd(qc, kc, vc, oc, lc, D ** -0.5, causal)
+        o_c[:, sl], lse_c[:, sl] = oc, lc
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    diff = [h for h in range(heads) if not (torch.equal(o[0, h], o_c[0, h]) and torch.equal(lse[0, h], lse_c[0, h]))]
+    assert not diff, f"{len(diff)} heads differ between one launch and small launches, first {diff[:5]}"
+    for h in (0, heads // 2, heads - 1):
+        qn, kn, vn = (x[:, h:h + 1].float().cpu().numpy() for x in (q, k, v))
+        o_ref, lse_ref = attention(qn, kn, vn, D ** -0.5, causal)
+        check_bf16(o[:, h:h + 1].float().cpu().numpy(), lse[:, h:h + 1].cpu().numpy(), o_ref, lse_ref,
+                   f"head {h} of {heads}, M={M} N={N} causal={causal}")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     """Failure detection without a fault: a kernel waits, with the kernels'
     bounded barrier wait, on a phase nothing completes. After 20 ms it gives
